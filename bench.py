@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged attention hot path on one GB300 (or N replicas).
+
+One step = one decode step over every layer of the workload: for each layer the
+slot write of the new tokens (pa_reshape_and_cache) followed by attention over
+the paged cache (pa_decode, or pa_mixed for a mixed batch), all captured in one
+CUDA graph.  Inputs are resident in HBM before timing starts.
+
+Printed (rank 0, one JSON line): KV GB/s = algorithmic K/V bytes the step must
+read (every cached token of every sequence, every KV head, every layer) divided
+by the step time; also sequence-steps/s, the fraction of HBM peak, the
+roofline of the decode kernel, an end-to-end number through the public API
+with host buffers, clocks seen during the timed region, and the CPU oracle's
+throughput on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_99_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and seq-steps/sec"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "qwen2.5-1.5b"
+DESCRIPTIONS = {
+    "tiny": "tiny decode: 1 layer, B=4, seq_lens 8/17/31/46, H_q=8, H_kv=2, d=128, block 16, bf16",
+    "qwen2.5-1.5b": "Qwen2.5-1.5B-shaped decode: 28 layers, B=64, H_q=12, H_kv=2, d=128, block 16, bf16, "
+                    "seq_lens~U[512,4096], random block placement",
+    "gqa40-8k": "40-layer GQA decode: B=40 at 8192 tokens, H_q=32, H_kv=8, d=128, block 16, fp16 KV",
+    "shared-prefix": "shared-prefix decode: 1 layer, B=128, H_q=32, H_kv=8, bf16, 128 aliased prefix blocks "
+                     "+ private suffix U[0,1000]",
+    "mixed-fp8": "mixed fp8: 1 layer, H_q=64, H_kv=8, e4m3 KV, 16 decode rows (lognormal median 8192, cap 32768) "
+                 "+ 2 prefill chunks of 512 on 4096-token contexts",
+}
+ELEM = {"bf16": 2, "fp16": 2, "fp8": 1}
+
+
+def kv_read_bytes(w: W.Workload) -> int:
+    """Algorithmic K/V bytes of one step: 2 * H_kv * d * b per cached token, per layer."""
+    return w.num_layers * int(w.seq_lens.sum().item()) * 2 * w.num_kv_heads * w.head_dim * ELEM[w.cache_dtype]
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (timing only; no data-path collective)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_99_gb300", "csrc")
+    for name in ("decode.cu", "pa_device.cuh", "pa_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was taken
+    on the current decode kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def build_step(w: W.Workload, pa, ws, outs, layers_caches, decode_only_kernels=False):
+    """Enqueue one step on the current stream (used inside graph capture)."""
+    for layer in range(w.num_layers):
+        kc, vc = layers_caches[layer]
+        ks = w.k_scale[layer:layer + 1] if w.k_scale is not None else None
+        vs = w.v_scale[layer:layer + 1] if w.v_scale is not None else None
+        if w.num_new_tokens and not decode_only_kernels:
+            pa.pa_reshape_and_cache(w.k_new[layer], w.v_new[layer], kc, vc, w.slot_mapping, ks, vs)
+        if w.is_decode_only:
+            pa.pa_decode(outs[layer], w.q[layer], kc, vc, w.block_tables, w.seq_lens, w.scale, ws, ks, vs)
+        else:
+            pa.pa_mixed(outs[layer], w.q[layer], w.query_start_loc, kc, vc, w.block_tables, w.seq_lens,
+                        w.max_q_len, w.scale, ws, ks, vs)
+
+
+def capture(fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()          # warm the library's per-device caches outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def run_ours(args, rank, world, local):
+    import paged_kv_cache_99_gb300 as pa
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.make(args.workload, dev)          # every replica runs the same workload (weak scaling)
+    layers_caches = [(w.k_cache[l], w.v_cache[l]) for l in range(w.num_layers)]
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, device=dev)
+    outs = [torch.empty_like(w.q[l]) for l in range(w.num_layers)]
+    kv_bytes = kv_read_bytes(w)
+    step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches))
+    decode_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, decode_only_kernels=True))
+    launches_per_step = w.num_layers * (2 if w.num_new_tokens else 1)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    unique_bytes = sum(c.numel() * c.element_size() * 2 for c in w.k_cache)
+    flush = unique_bytes < 2 * l2
+    flush_buf = torch.empty(4 * l2, dtype=torch.uint8, device=dev) if flush else None
+
+    def one_step():
+        if flush:
+            flush_buf.fill_(1)
+        step_graph.replay()
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    status = pa.pa_read_device_status(ws)
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device status after warm-up: {pa.pa_status_string(status)}")
+
+    # ---- timed region: K steps, per-step device time by events ----
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(1)
+        ev[i][0].record()
+        step_graph.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = reduce_max(ms_local, world)
+
+    # ---- decode kernel alone, same inputs: average launch duration ----
+    dg_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(1)
+        dg_ev[i][0].record()
+        decode_graph.replay()
+        dg_ev[i][1].record()
+    torch.cuda.synchronize()
+    dec_ms = sum(a.elapsed_time(b) for a, b in dg_ev) / args.steps / w.num_layers
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(args, w, pa, ws, outs, layers_caches, dev) if not args.no_e2e else None
+
+    peaks, peak_src = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    value = kv_bytes * world / (ms * 1e-3) / 1e9
+    per_launch_bytes = kv_bytes / w.num_layers
+    achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.cache_dtype,
+        "data": "synthetic",
+        "config": {
+            "workload": DESCRIPTIONS.get(args.workload, args.workload),
+            "name": args.workload,
+            "kv_bytes_per_step": kv_bytes,
+            "launch": f"one CUDA graph per step: {w.num_layers} x ("
+                      + ("pa_reshape_and_cache + " if w.num_new_tokens else "")
+                      + ("pa_decode" if w.is_decode_only else "pa_mixed") + ")",
+            "l2": ("L2 flushed between steps" if flush else
+                   f"inputs larger than L2 ({unique_bytes / 1e9:.2f} GB of cache vs {l2 / 1e6:.0f} MB L2)"),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "seq_steps_per_s": round(w.num_seqs * world / (ms * 1e-3), 1),
+        "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * value / world / hbm_peak, 2),
+        "roofline": {
+            "kernel": "pa_decode" if w.is_decode_only else "pa_mixed decode rows",
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": hbm_peak,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": per_launch_bytes,
+            "avg_launch_ms": round(dec_ms, 5),
+        },
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"]["kv_bytes_per_step"] = kv_bytes
+    return line
+
+
+def run_e2e(args, w, pa, ws, outs, layers_caches, dev):
+    """Same metric through the public API, with the step's inputs copied from pinned
+    host memory and the outputs copied back inside the timed region."""
+    host_in = [w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables, w.seq_lens, w.query_start_loc]
+    pinned = [t.detach().cpu().pin_memory() for t in host_in]
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    g = capture(lambda: build_step(w, pa, ws, outs, layers_caches))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for dst, src in zip(host_in, pinned):
+            dst.copy_(src, non_blocking=True)
+        g.replay()
+        for dst, src in zip(host_out, outs):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    return {"value": round(kv_read_bytes(w) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+CODE = {"bf16": 0, "fp16": 1, "fp8": 2}
+
+
+def raw(t: torch.Tensor) -> np.ndarray:
+    """Storage bits of a tensor as numpy (uint16 for 16-bit types, uint8 for FP8)."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def cpu_baseline(w: W.Workload, seconds: float, total_layers: int | None = None):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    workload: whole layers (slot write + attention for every sequence) until
+    `seconds` of oracle time have passed; reported in the same unit (KV GB/s)."""
+    import oracle
+    per_layer = kv_read_bytes(w) // w.num_layers
+    qsl = w.query_start_loc.cpu().numpy()
+    tables = w.block_tables.cpu().numpy()
+    lens = w.seq_lens.cpu().numpy()
+    slots = w.slot_mapping.cpu().numpy()
+    elapsed, layers = 0.0, 0
+    while layers < w.num_layers and (layers == 0 or elapsed < seconds):
+        kc, vc = raw(w.k_cache[layers]), raw(w.v_cache[layers])
+        ks = float(w.k_scale[layers]) if w.k_scale is not None else 1.0
+        vs = float(w.v_scale[layers]) if w.v_scale is not None else 1.0
+        qb = raw(w.q[layers])
+        kn, vn = raw(w.k_new[layers]), raw(w.v_new[layers])
+        t1 = time.perf_counter()
+        if w.num_new_tokens:
+            kc, vc = oracle.reshape_and_cache(kn, vn, CODE[w.q_dtype], kc, vc, CODE[w.cache_dtype], slots, ks, vs)
+        if w.is_decode_only:
+            oracle.decode(qb, CODE[w.q_dtype], kc, vc, CODE[w.cache_dtype], tables, lens, w.scale, ks, vs)
+        else:
+            oracle.mixed(qb, CODE[w.q_dtype], qsl, kc, vc, CODE[w.cache_dtype], tables, lens, w.scale, ks, vs)
+        elapsed += time.perf_counter() - t1
+        layers += 1
+    return {"value": round(layers * per_layer / elapsed / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{layers} of {total_layers or w.num_layers} layers, every sequence, slot write + attention, "
+                      f"float64, one thread (host has {os.cpu_count()} cores)",
+            "seconds": round(elapsed, 3)}
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores, same workload, metric and unit; each step a
+    bounded sample (whole layers)."""
+    if rank != 0:
+        return None
+    kw = {"num_layers": 1} if args.workload in ("qwen2.5-1.5b", "gqa40-8k") else {}
+    w = W.make(args.workload, "cpu", **kw)
+    total = {"qwen2.5-1.5b": 28, "gqa40-8k": 40}.get(args.workload, w.num_layers)
+    per_step = []
+    for _ in range(args.warmup + args.steps):
+        per_step.append(cpu_baseline(w, args.ref_step_seconds, total))
+    timed = per_step[args.warmup:]
+    value = statistics.mean(x["value"] for x in timed)
+    ms = statistics.mean(1e3 * x["seconds"] for x in timed)
+    cb = dict(timed[-1])
+    cb["value"] = round(value, 4)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS.get(args.workload, args.workload), "name": args.workload},
+        "cpu_baseline": cb,
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.NAMED))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

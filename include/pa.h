@@ -1,0 +1,209 @@
+/*
+ * pa.h -- C ABI of the paged-KV-cache attention library (libpa.so), sm_103a.
+ *
+ * The operations follow the statement of the problem on three web pages:
+ *   [P1] "Basics of LLM Inference and vLLM Internals: KV Cache, PagedAttention,
+ *        and Scheduler" -- s.2 "KV Cache and Sizing Formulas", s.4 "PagedAttention
+ *        and Block Management", s.6 "Chunked Prefill, Scheduler, and Preemption";
+ *   [P2] drpranayjha.com (Red Hat AI Inference Server part) -- "How PagedAttention
+ *        pages the KV cache";
+ *   [P3] "The Memory Trick Behind Fast LLM Serving" -- "PagedAttention changes
+ *        the shape of the problem", "Batching does not merge the conversations".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.   Every pointer argument named as "device" is caller-owned GPU memory
+ *           of the current device; the library allocates no memory, keeps no
+ *           state besides per-device attribute caches, and never synchronises
+ *           the stream (except pa_read_device_status, which says so).
+ * Streams.  Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *           stream).  pa_stream_t is the same handle as cudaStream_t.
+ * Errors.   Host-checkable problems are reported before anything is launched:
+ *           PA_ERR_INVALID_ARG (null pointer, negative count, misaligned buffer,
+ *           H_q not a multiple of H_kv, ...), PA_ERR_UNSUPPORTED (head_dim != 128,
+ *           block_size != 16, dtype pair not listed), PA_ERR_WORKSPACE (workspace
+ *           too small).  A failed launch returns PA_ERR_CUDA.  Problems only the
+ *           device can see (a block-table entry outside the pool, a bounded wait
+ *           that ran out) are recorded in the workspace's status word and
+ *           returned by pa_read_device_status; kernels never trap.
+ * Shapes.   head_dim d = 128 and block_size = 16 only.  Cache layout is
+ *           [num_blocks][num_kv_heads][16][128] for both K and V, so one
+ *           (block, KV head) tile is 16 x 128 contiguous elements (4 KiB in
+ *           bf16/fp16, 2 KiB in FP8).  A slot number is
+ *           physical_block * 16 + offset.
+ * GQA.      Query head h reads KV head h / (num_q_heads / num_kv_heads):
+ *           consecutive query heads form a group [P1 s.2].
+ * FP8.      FP8-E4M3 ("fn": bias 7, max 448, no inf, NaN = S.1111.111) with one
+ *           float32 scale per tensor, separate for K and V, read from device
+ *           memory so that calls can be captured in CUDA graphs.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,
+    PA_ERR_UNSUPPORTED = 2,
+    PA_ERR_CUDA = 3,
+    PA_ERR_TIMEOUT = 4,        /* device: a bounded wait gave up */
+    PA_ERR_OUT_OF_RANGE = 5,   /* device: a block-table entry outside [0, num_blocks) */
+    PA_ERR_WORKSPACE = 6
+} pa_status;
+
+typedef enum { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
+
+/* Static description of a status code.  Never NULL. */
+PA_API const char* pa_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+PA_API int pa_version(void);
+
+/*
+ * Slot write ("reshape_and_cache") [P1 s.4 block table; P3 "PagedAttention
+ * changes the shape of the problem"].
+ *
+ * For every new token t in [0, num_tokens) with slot = slot_mapping[t] >= 0,
+ * stores k[t][h][:] into k_cache[slot / 16][h][slot % 16][:] and v[t][h][:]
+ * into v_cache at the same place, for every KV head h.  A negative slot is
+ * padding and writes nothing.  A slot >= num_blocks * 16 is skipped (nothing is
+ * written).  Two tokens with the same slot in one call: undefined which wins.
+ *
+ *   k, v           device, [num_tokens][num_kv_heads][128] of src_dtype (bf16|fp16)
+ *   k_cache,v_cache device, [num_blocks][num_kv_heads][16][128] of cache_dtype,
+ *                  16-byte aligned
+ *   slot_mapping   device, int64 [num_tokens]
+ *   cache_dtype    == src_dtype (bits copied unchanged), or PA_FP8_E4M3:
+ *                  code = e4m3(fl32(x) / scale), the quotient rounded once to
+ *                  binary32 (IEEE division), then round-to-nearest-even to E4M3 with
+ *                  magnitudes above 448 clamped to 448; NaN -> S.1111.111 (sign
+ *                  kept); -0 -> 0x80 [P1 s.2, s.7 "--kv-cache-dtype fp8"].
+ *   k_scale,v_scale device float32 scalars; required (non-NULL) iff FP8.
+ * Bytes outside the written slots are never touched.
+ */
+PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, pa_dtype src_dtype,
+                               pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                               pa_stream_t stream);
+
+/*
+ * Bytes of workspace pa_decode / pa_mixed need on the CURRENT device for
+ * num_seqs sequences (the default worker count depends on the device's SM
+ * count).  The workspace is caller-owned device memory, 256-byte aligned, that
+ * must be ZERO-FILLED once after allocation; every call that returns PA_OK and
+ * completes on the device leaves it in that state again (apart from the status
+ * word, see pa_read_device_status).  After a device-side PA_ERR_TIMEOUT, zero it
+ * again.  One workspace must not be used by two calls that may overlap on the
+ * GPU.  Returns 0 for invalid arguments.
+ */
+PA_API size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
+
+/* Default number of decode workers (warps) on the current device. */
+PA_API int pa_default_workers(void);
+
+/*
+ * Decode attention over the paged cache [P1 s.2 "attention revisits the keys
+ * and values of all preceding tokens", s.4 block table; P2 "How PagedAttention
+ * pages the KV cache"].
+ *
+ * For every sequence s and query head h (KV head kh = h / G, G = H_q / H_kv):
+ *   out[s][h][:] = softmax_t( scale * q[s][h] . K_s[t] ) . V_s[t],  t < seq_lens[s]
+ * where token t of sequence s lives in physical block block_tables[s][t / 16],
+ * offset t % 16, KV head kh.  seq_lens[s] counts every cached token, including
+ * this step's own (write it with pa_reshape_and_cache first).  seq_lens[s] == 0
+ * gives zeros.  Entries of block_tables past ceil(seq_lens[s] / 16) are never
+ * read.  An entry that is read and lies outside [0, num_blocks) is replaced by
+ * block 0 and recorded as PA_ERR_OUT_OF_RANGE in the workspace status word.
+ *
+ *   out            device, [num_seqs][num_q_heads][128] of q_dtype
+ *   q              device, [num_seqs][num_q_heads][128], q_dtype bf16|fp16, 16-byte aligned
+ *   k_cache,v_cache device, layout above; cache_dtype == q_dtype or PA_FP8_E4M3
+ *   block_tables   device, int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens       device, int32 [num_seqs]; each <= 16 * max_blocks_per_seq
+ *   scale          softmax scale (e.g. 1/sqrt(128))
+ *   k_scale,v_scale device float32 scalars, required iff cache is FP8 (dequant
+ *                  is code * scale)
+ *   workspace      see pa_workspace_size
+ * num_seqs <= 8192.  The work is split evenly over the workers by cached
+ * blocks (long sequences are split across workers and merged with a
+ * log-sum-exp combine), so the result does not depend on where blocks live.
+ */
+PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                    const float* k_scale, const float* v_scale, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
+
+/* pa_decode with an explicit worker count (1 .. pa_default_workers(); 0 = the
+ * default).  Fewer workers means longer ranges per worker and fewer split
+ * points; results agree with pa_decode to rounding. */
+PA_API pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                       int head_dim, int block_size, int num_blocks, float scale,
+                       pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
+                       const float* v_scale, void* workspace, size_t workspace_bytes,
+                       int num_workers, pa_stream_t stream);
+
+/*
+ * Mixed batch: decode rows and prefill chunks in one flattened query array
+ * [P3 "Batching does not merge the conversations"; P1 s.6 chunked prefill].
+ *
+ * Sequence s owns query rows query_start_loc[s] .. query_start_loc[s+1]-1
+ * (q_len_s rows).  seq_lens[s] counts the cached tokens including this step's
+ * q_len_s new ones, so row j of sequence s sits at position
+ * pos = seq_lens[s] - q_len_s + j and attends causally to tokens 0 .. pos of its
+ * own sequence only.  q_len_s == 1 is a decode row; q_len_s == 0 contributes
+ * nothing.
+ *
+ *   out, q          device, [total_q][num_q_heads][128] of q_dtype
+ *   query_start_loc device, int32 [num_seqs + 1], non-decreasing,
+ *                   query_start_loc[0] == 0, query_start_loc[num_seqs] == total_q
+ *   max_q_len       host upper bound of q_len_s (sizes the prefill grid)
+ * Other arguments as pa_decode.
+ */
+PA_API pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
+                   const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* seq_lens, int num_seqs, int total_q, int max_q_len,
+                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   float scale, pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
+                   const float* v_scale, void* workspace, size_t workspace_bytes,
+                   pa_stream_t stream);
+
+/*
+ * Reads (and clears) the device-side status word of a workspace.  Synchronises
+ * `stream`.  Returns PA_OK, PA_ERR_OUT_OF_RANGE or PA_ERR_TIMEOUT (the first
+ * recorded, timeouts first), or PA_ERR_CUDA if the copy failed.
+ */
+PA_API pa_status pa_read_device_status(void* workspace, pa_stream_t stream);
+
+/*
+ * Self-test of the bounded waits: launches one warp that waits on a barrier
+ * nothing will ever complete, with a limit of timeout_us microseconds; the wait
+ * must give up and record PA_ERR_TIMEOUT in the workspace status word (read it
+ * with pa_read_device_status).  Touches only the status word.
+ */
+PA_API pa_status pa_selftest_wait_timeout(void* workspace, size_t workspace_bytes, unsigned timeout_us,
+                                   pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,190 @@
+"""Paged-KV-cache attention on one GB300 (sm_103a): a thin ctypes binding of libpa.so.
+
+Every function here only marshals torch tensors into the C ABI declared in
+``include/pa.h`` (pointers, sizes, dtypes, the current CUDA stream) and raises
+``PagedAttentionError`` on a non-zero status; all the work runs in the
+library's CUDA kernels.  There is no CPU fallback: if libpa.so is missing the
+import of the binding fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build_ext
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_TIMEOUT, PA_ERR_OUT_OF_RANGE, \
+    PA_ERR_WORKSPACE = range(7)
+PA_BF16, PA_FP16, PA_FP8_E4M3 = 0, 1, 2
+
+_DTYPE = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.uint8: PA_FP8_E4M3,
+          torch.float8_e4m3fn: PA_FP8_E4M3}
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib().pa_status_string(status).decode()} (status {status})")
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return build_ext.LIB_PATH
+
+
+def _lib():
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = build_ext.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"libpa.so is not built ({path}); run __graft_entry__.build() "
+                          "or python -m paged_kv_cache_99_gb300.build_ext")
+    lib = ctypes.CDLL(path)
+    P, I, Z, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    lib.pa_status_string.argtypes = [I]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_version.argtypes = []
+    lib.pa_version.restype = I
+    lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
+    lib.pa_reshape_and_cache.restype = I
+    lib.pa_workspace_size.argtypes = [I, I, I, I]
+    lib.pa_workspace_size.restype = Z
+    lib.pa_default_workers.argtypes = []
+    lib.pa_default_workers.restype = I
+    lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
+    lib.pa_decode.restype = I
+    lib.pa_decode_ex.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, I, P]
+    lib.pa_decode_ex.restype = I
+    lib.pa_mixed.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
+    lib.pa_mixed.restype = I
+    lib.pa_read_device_status.argtypes = [P, P]
+    lib.pa_read_device_status.restype = I
+    lib.pa_selftest_wait_timeout.argtypes = [P, Z, ctypes.c_uint, P]
+    lib.pa_selftest_wait_timeout.restype = I
+    _LIB = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtypes=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedAttentionError(status, what)
+
+
+def pa_version() -> int:
+    return _lib().pa_version()
+
+
+def pa_status_string(status: int) -> str:
+    return _lib().pa_status_string(status).decode()
+
+
+def pa_default_workers() -> int:
+    return _lib().pa_default_workers()
+
+
+def pa_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128) -> int:
+    return int(_lib().pa_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim))
+
+
+def new_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, device=None) -> torch.Tensor:
+    """Zero-filled workspace of pa_workspace_size bytes on the current device."""
+    n = pa_workspace_size(num_seqs, num_q_heads, num_kv_heads)
+    if n == 0:
+        raise ValueError("invalid workspace arguments")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None, stream=None):
+    """Slot write: k, v [T, H_kv, 128] -> caches [num_blocks, H_kv, 16, 128] at slot_mapping[T] (int64)."""
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t, n, (torch.bfloat16, torch.float16))
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, tuple(_DTYPE))
+    _need(slot_mapping, "slot_mapping", (torch.int64,))
+    T, H, d = k.shape
+    nb, H2, bs, d2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or H2 != H or d2 != d or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch")
+    st = _lib().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, H, d,
+                                     bs, nb, _DTYPE[k.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale),
+                                     _ptr(v_scale), _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, workspace, k_scale=None, v_scale=None,
+              num_workers: int = 0, stream=None):
+    """Decode attention: q, out [B, H_q, 128]; block_tables int32 [B, max_blocks]; seq_lens int32 [B]."""
+    _need(q, "q", (torch.bfloat16, torch.float16))
+    _need(out, "out", (q.dtype,))
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, tuple(_DTYPE))
+    _need(block_tables, "block_tables", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(workspace, "workspace", (torch.uint8,))
+    B, Hq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    if out.shape != q.shape or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    st = _lib().pa_decode_ex(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                             block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, d, bs, nb, float(scale),
+                             _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale), _ptr(v_scale),
+                             _ptr(workspace), workspace.numel(), int(num_workers), _stream(stream))
+    _check(st, "pa_decode")
+
+
+def pa_mixed(out, q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, max_q_len, scale, workspace,
+             k_scale=None, v_scale=None, stream=None):
+    """Mixed decode rows + causal prefill chunks: q, out [total_q, H_q, 128]; query_start_loc int32 [B+1]."""
+    _need(q, "q", (torch.bfloat16, torch.float16))
+    _need(out, "out", (q.dtype,))
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, tuple(_DTYPE))
+    _need(query_start_loc, "query_start_loc", (torch.int32,))
+    _need(block_tables, "block_tables", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(workspace, "workspace", (torch.uint8,))
+    total_q, Hq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    B = seq_lens.shape[0]
+    if out.shape != q.shape or block_tables.shape[0] != B or query_start_loc.shape != (B + 1,):
+        raise ValueError("shape mismatch")
+    st = _lib().pa_mixed(_ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
+                         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, total_q, int(max_q_len), Hq,
+                         Hkv, d, bs, nb, float(scale), _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale),
+                         _ptr(v_scale), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "pa_mixed")
+
+
+def pa_read_device_status(workspace, stream=None) -> int:
+    """Device status word of a workspace (synchronises the stream, clears the word)."""
+    _need(workspace, "workspace", (torch.uint8,))
+    return int(_lib().pa_read_device_status(_ptr(workspace), _stream(stream)))
+
+
+def pa_selftest_wait_timeout(workspace, timeout_us: int, stream=None) -> None:
+    _need(workspace, "workspace", (torch.uint8,))
+    _check(_lib().pa_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(timeout_us), _stream(stream)),
+           "pa_selftest_wait_timeout")

@@ -1,0 +1,571 @@
+// Paged decode attention for sm_103a.
+//
+// Problem ("Basics of LLM Inference and vLLM Internals", s.2 and s.4; "The
+// Memory Trick Behind Fast LLM Serving", "PagedAttention changes the shape of
+// the problem"): one query token per sequence attends to every cached token of
+// that sequence; token t lives in physical block block_tables[s][t / 16] at
+// offset t % 16; the query heads of a GQA group share one KV head.
+//
+// Design (one GB300, HBM-bound):
+//  * Work unit = (sequence, KV head, group of <= 8 query heads).  The cached
+//    blocks of all units are laid end to end and cut into equal contiguous
+//    ranges, one per warp, so every warp streams the same number of 4 KiB tiles
+//    whatever the length mix; a unit cut by a range boundary is merged by a
+//    log-sum-exp combine done by whichever warp finishes the unit last (ticket).
+//  * Each warp owns a ring of stages in shared memory.  One lane issues bulk
+//    tensor copies (TMA, 128-byte swizzle) of the K and V tiles of a physical
+//    block straight from the block table; the ring keeps several tiles per warp
+//    in flight.  Block-table entries are fetched 32 at a time by the warp.
+//  * Per 16-key block the warp computes S^T = K . Q^T with keys as the MMA M
+//    dimension (16 keys = one block) and the <= 8 query heads of the group as N,
+//    so no MMA row is padding when G = 8.  After an online softmax, the
+//    probabilities are transposed in registers (movmatrix) into the B operand of
+//    O^T = V^T . P^T, whose accumulator columns are again the heads.
+//  * FP8-E4M3 tiles are widened to fp16 exactly on the fly (cvt e4m3x2) and the
+//    per-tensor scales are folded into the softmax scale and the final divide.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+template <int Kind>
+struct DecodeCfg {
+    static constexpr bool kFp8 = Kind == kKindFp8;
+    static constexpr int kTileBytes = kFp8 ? 2048 : 4096;   // one (block, head) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;      // K then V
+    static constexpr int kStages = kFp8 ? 6 : 3;
+    static constexpr int kTileArea = kDecodeWarps * kStages * kStageBytes;
+    static constexpr int kBarBytes = kDecodeWarps * kStages * 8;
+};
+
+// Flattened-order cursor over (sequence, unit-in-sequence, block).
+struct Cursor {
+    int s;    // sequence
+    int uh;   // KV head * head_groups + head group
+    int j;    // logical block
+    int nb;   // blocks of sequence s
+};
+
+__device__ __forceinline__ void cursor_advance(Cursor& c, const int* cum, int B, int UH) {
+    if (++c.j == c.nb) {
+        c.j = 0;
+        if (++c.uh == UH) {
+            c.uh = 0;
+            do {
+                ++c.s;
+            } while (c.s < B && cum[c.s + 1] == cum[c.s]);
+            if (c.s < B) c.nb = (cum[c.s + 1] - cum[c.s]) / UH;
+        }
+    }
+}
+
+// Worker (warp) whose range holds flattened index f, for T indices over W workers
+// with range w = [floor(w T / W), floor((w + 1) T / W)).
+__device__ __forceinline__ int worker_of(long long f, long long T, int W) {
+    return static_cast<int>(((f + 1) * W - 1) / T);
+}
+
+template <typename T>
+__device__ __forceinline__ T shfl(T v, int src) {
+    return __shfl_sync(0xffffffffu, v, src);
+}
+
+}  // namespace
+
+template <int Kind, bool QBf16>
+__global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const DecodeParams p) {
+    using Cfg = DecodeCfg<Kind>;
+    constexpr bool kFp8 = Cfg::kFp8;
+    constexpr bool kMmaBf16 = Kind == kKindBf16;   // fp16 and FP8 (widened) use f16 MMA
+    constexpr int NS = Cfg::kStages;
+    constexpr int TILE = Cfg::kTileBytes;
+    constexpr int STAGE = Cfg::kStageBytes;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int warp_tot[kDecodeWarps];
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t tiles = (raw_base + 1023u) & ~1023u;     // 128-byte swizzle needs 1 KiB alignment
+    uint8_t* aligned = smem_raw + (tiles - raw_base);
+    const uint32_t bars = tiles + Cfg::kTileArea;
+    int* cum = reinterpret_cast<int*>(aligned + Cfg::kTileArea + Cfg::kBarBytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t my_tiles = tiles + warp * NS * STAGE;
+    const uint32_t my_bars = bars + warp * NS * 8;
+
+    if (lane == 0) {
+        for (int st = 0; st < NS; ++st) mbar_init(my_bars + 8 * st, 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 0) {
+        tmap_prefetch(&kmap);
+        tmap_prefetch(&vmap);
+    }
+
+    grid_dependency_wait();
+
+    const int B = p.num_seqs;
+    const int UH = p.num_kv_heads * p.head_groups;
+    const bool mixed = p.query_start_loc != nullptr;
+
+    // ---- prologue: blocks per unit of every sequence, exclusive scan -> cum ----
+    auto eligible = [&](int s) -> bool {
+        return !mixed || (p.query_start_loc[s + 1] - p.query_start_loc[s] == 1);
+    };
+    auto unit_blocks = [&](int s) -> int {
+        if (!eligible(s)) return 0;
+        int n = p.seq_lens[s];
+        int nb = (max(n, 0) + kBlockSize - 1) / kBlockSize;
+        return min(nb, p.max_blocks) * UH;
+    };
+    {
+        const int per = (B + blockDim.x - 1) / blockDim.x;
+        const int beg = min(B, static_cast<int>(threadIdx.x) * per);
+        const int end = min(B, beg + per);
+        int local = 0;
+        for (int s = beg; s < end; ++s) local += unit_blocks(s);
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int run = incl - local;
+        for (int w = 0; w < warp; ++w) run += warp_tot[w];
+        for (int s = beg; s < end; ++s) {
+            cum[s] = run;
+            run += unit_blocks(s);
+        }
+        if (threadIdx.x == blockDim.x - 1) cum[B] = run;
+    }
+    // empty decode rows produce zeros; over-long sequences are an input error
+    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+        if (!eligible(s)) continue;
+        const int n = p.seq_lens[s];
+        if (threadIdx.x == 0 && n > p.max_blocks * kBlockSize) atomicOr(p.status, kDevErrRange);
+        if (n > 0) continue;
+        const int row = mixed ? p.query_start_loc[s] : s;
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                            static_cast<size_t>(row) * p.num_q_heads * kHeadDim);
+        for (int i = threadIdx.x; i < p.num_q_heads * kHeadDim / 8; i += blockDim.x)
+            o[i] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    grid_launch_dependents();
+
+    const long long T = cum[B];
+    const int W = p.num_workers;
+    const int wid = blockIdx.x * kDecodeWarps + warp;
+    if (wid >= W || T == 0) return;
+    const long long f0 = T * wid / W;
+    const long long f1 = T * (wid + 1) / W;
+    if (f0 == f1) return;
+    const int nblk = static_cast<int>(f1 - f0);
+
+    // locate f0: sequence with cum[s] <= f0 < cum[s+1]
+    Cursor start;
+    {
+        int lo = 0, hi = B;
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (cum[mid] <= f0) lo = mid; else hi = mid;
+        }
+        start.s = lo;
+        start.nb = (cum[lo + 1] - cum[lo]) / UH;
+        const int rem = static_cast<int>(f0 - cum[lo]);
+        start.uh = rem / start.nb;
+        start.j = rem % start.nb;
+    }
+
+    // per-lane fragment geometry
+    const int g = lane >> 2;           // MMA group row
+    const int t = lane & 3;            // MMA thread in group
+    const int mi = lane >> 3;          // ldmatrix sub-matrix this lane addresses
+    const int r8 = lane & 7;           // row within it
+    const uint32_t k_row = static_cast<uint32_t>(r8 + ((mi & 1) << 3));
+    const uint32_t v_row = kFp8 ? k_row : static_cast<uint32_t>(r8 + ((mi >> 1) << 3));
+
+    // ---- producer: block-table window + TMA issue ----
+    int tbl_s = -1, tbl_j0 = -1, tbl = 0;
+    auto issue = [&](const Cursor& c, int k) {
+        if (c.s != tbl_s || (c.j & ~31) != tbl_j0) {
+            tbl_s = c.s;
+            tbl_j0 = c.j & ~31;
+            const int jj = tbl_j0 + lane;
+            tbl = jj < c.nb ? __ldg(p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + jj) : 0;
+        }
+        int phys = shfl(tbl, c.j & 31);
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+            if (lane == 0) atomicOr(p.status, kDevErrRange);
+            phys = 0;
+        }
+        const int h = c.uh / p.head_groups;
+        const int y = (phys * p.num_kv_heads + h) * kBlockSize;
+        if (lane == 0) {
+            const int st = k % NS;
+            const uint32_t bar = my_bars + 8 * st;
+            const uint32_t dst = my_tiles + st * STAGE;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, STAGE);
+            if constexpr (kFp8) {
+                tma_load_2d(dst, &kmap, 0, y, bar);
+                tma_load_2d(dst + TILE, &vmap, 0, y, bar);
+            } else {
+                tma_load_2d(dst, &kmap, 0, y, bar);
+                tma_load_2d(dst + 2048, &kmap, 64, y, bar);
+                tma_load_2d(dst + TILE, &vmap, 0, y, bar);
+                tma_load_2d(dst + TILE + 2048, &vmap, 64, y, bar);
+            }
+        }
+    };
+
+    Cursor P = start;
+    int kp = 0;
+    for (; kp < NS && kp < nblk; ++kp) {
+        issue(P, kp);
+        cursor_advance(P, cum, B, UH);
+    }
+
+    const float kscale = kFp8 ? __ldg(p.k_scale) : 1.0f;
+    const float vscale = kFp8 ? __ldg(p.v_scale) : 1.0f;
+    const float s_log2 = p.scale_log2 * kscale;
+
+    Cursor C = start;
+    float o[8][4];
+    uint32_t qf[8][2];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int n_cur = 0, row_cur = 0;
+    bool open = false;
+
+    for (int kc = 0; kc < nblk; ++kc) {
+        if (!open) {
+            // ---- segment start: query fragments of this unit ----
+            open = true;
+            n_cur = p.seq_lens[C.s];
+            row_cur = mixed ? p.query_start_loc[C.s] : C.s;
+            const int h = C.uh / p.head_groups;
+            const int hg = C.uh % p.head_groups;
+            const int gh = hg * kHeadsPerGroup + g;        // head within the GQA group
+            const bool live = gh < p.group;
+            const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
+                                   (static_cast<size_t>(row_cur) * p.num_q_heads + h * p.group + (live ? gh : 0)) * kHeadDim;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                if constexpr (!kFp8) {
+                    qf[kk][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * t) : 0u;
+                    qf[kk][1] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * t + 8) : 0u;
+                } else {
+                    // k-slots (2t, 2t+1) <-> d (16kk+4t, +1); (2t+8, 2t+9) <-> d (16kk+4t+2, +3)
+                    uint2 raw = live ? *reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * t) : make_uint2(0, 0);
+                    qf[kk][0] = pack2<false>(to_float<QBf16>(raw.x & 0xffff), to_float<QBf16>(raw.x >> 16));
+                    qf[kk][1] = pack2<false>(to_float<QBf16>(raw.y & 0xffff), to_float<QBf16>(raw.y >> 16));
+                }
+            }
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+
+        // ---- wait for this block's tiles ----
+        const int st = kc % NS;
+        const uint32_t bar = my_bars + 8 * st;
+        const uint32_t parity = (kc / NS) & 1;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(bar, parity, p.timeout_ns);
+        ok = shfl(static_cast<int>(ok), 0) != 0;
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(p.status, kDevErrTimeout);
+                // let copies still in flight land before the warp leaves
+                for (int k = kc; k < kp; ++k)
+                    mbar_wait_bounded(my_bars + 8 * (k % NS), (k / NS) & 1, p.timeout_ns);
+            }
+            __syncwarp();
+            return;
+        }
+        mbar_try_wait(bar, parity);   // phase is complete: acquire for every lane
+
+        const uint32_t kt = my_tiles + st * STAGE;
+        const uint32_t vt = kt + TILE;
+        const int valid = min(kBlockSize, n_cur - C.j * kBlockSize);
+
+        // ---- S^T = K . Q^T : rows = 16 keys, cols = 8 heads ----
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (!kFp8) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t c = 2 * kk + (mi >> 1);
+                const uint32_t addr = kt + ((c >> 3) << 11) + (k_row << 7) + (((c & 7) ^ r8) << 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(addr, a0, a1, a2, a3);
+                if (kk & 1) mma16816<kMmaBf16>(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                else        mma16816<kMmaBf16>(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            }
+        } else {
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const uint32_t c = 2 * kq + (mi >> 1);
+                const uint32_t addr = kt + (k_row << 7) + ((c ^ r8) << 4);
+                uint32_t x0, x1, x2, x3;
+                ldsm_x4(addr, x0, x1, x2, x3);
+                mma16816<false>(sa, e4m3x2_to_f16x2(x0 & 0xffff), e4m3x2_to_f16x2(x1 & 0xffff),
+                                e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16), qf[2 * kq][0],
+                                qf[2 * kq][1]);
+                mma16816<false>(sb, e4m3x2_to_f16x2(x2 & 0xffff), e4m3x2_to_f16x2(x3 & 0xffff),
+                                e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16), qf[2 * kq + 1][0],
+                                qf[2 * kq + 1][1]);
+            }
+        }
+        // element (key g | g+8, head 2t | 2t+1), in log2 units
+        float s0 = (sa[0] + sb[0]) * s_log2;
+        float s1 = (sa[1] + sb[1]) * s_log2;
+        float s2 = (sa[2] + sb[2]) * s_log2;
+        float s3 = (sa[3] + sb[3]) * s_log2;
+        if (valid < kBlockSize) {
+            if (g >= valid) s0 = s1 = -INFINITY;
+            if (g + 8 >= valid) s2 = s3 = -INFINITY;
+        }
+
+        // ---- online softmax over keys (lanes with equal t share heads) ----
+        float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o2));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o2));
+        }
+        const float mn0 = fmaxf(m0, x0), mn1 = fmaxf(m1, x1);
+        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+        const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+            o[dt][0] *= al0;
+            o[dt][1] *= al1;
+            o[dt][2] *= al0;
+            o[dt][3] *= al1;
+        }
+        // P^T as the B operand: keys 2t,2t+1 (and +8) of head g
+        const uint32_t pb0 = movmatrix_t(pack2<kMmaBf16>(p0, p1));
+        const uint32_t pb1 = movmatrix_t(pack2<kMmaBf16>(p2, p3));
+
+        // keys beyond the sequence end: zero V so stale or NaN slots cannot leak
+        uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+        if (valid < kBlockSize) {
+            vm01 = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+            vm23 = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
+        }
+
+        // ---- O^T += V^T . P^T : rows = d, cols = heads ----
+        if constexpr (!kFp8) {
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                const uint32_t c = 2 * dt + (mi & 1);
+                const uint32_t addr = vt + ((c >> 3) << 11) + (v_row << 7) + (((c & 7) ^ r8) << 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(addr, a0, a1, a2, a3);
+                mma16816<kMmaBf16>(o[dt], a0 & vm01, a1 & vm01, a2 & vm23, a3 & vm23, pb0, pb1);
+            }
+        } else {
+#pragma unroll
+            for (int dq = 0; dq < 4; ++dq) {
+                const uint32_t c = 2 * dq + (mi >> 1);
+                const uint32_t addr = vt + (v_row << 7) + ((c ^ r8) << 4);
+                uint32_t x0v, x1v, x2v, x3v;
+                ldsm_x4_t(addr, x0v, x1v, x2v, x3v);
+                // bytes [V(2t,d), V(2t,d+1), V(2t+1,d), V(2t+1,d+1)], d = 16c + 2g
+                const uint32_t e0 = prmt(x0v, 0, 0x3120), e1 = prmt(x1v, 0, 0x3120);
+                const uint32_t e2 = prmt(x2v, 0, 0x3120), e3 = prmt(x3v, 0, 0x3120);
+                mma16816<false>(o[2 * dq], e4m3x2_to_f16x2(e0 & 0xffff) & vm01,
+                                e4m3x2_to_f16x2(e0 >> 16) & vm01, e4m3x2_to_f16x2(e1 & 0xffff) & vm23,
+                                e4m3x2_to_f16x2(e1 >> 16) & vm23, pb0, pb1);
+                mma16816<false>(o[2 * dq + 1], e4m3x2_to_f16x2(e2 & 0xffff) & vm01,
+                                e4m3x2_to_f16x2(e2 >> 16) & vm01, e4m3x2_to_f16x2(e3 & 0xffff) & vm23,
+                                e4m3x2_to_f16x2(e3 >> 16) & vm23, pb0, pb1);
+            }
+        }
+        __syncwarp();
+
+        // refill the stage just consumed
+        if (kp < nblk) {
+            issue(P, kp);
+            cursor_advance(P, cum, B, UH);
+            ++kp;
+        }
+
+        // ---- segment end: unit finished or range finished ----
+        if (C.j == C.nb - 1 || kc == nblk - 1) {
+            open = false;
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
+            }
+            const int u = C.s * UH + C.uh;
+            const long long fu = cum[C.s] + static_cast<long long>(C.uh) * C.nb;
+            const int wa = worker_of(fu, T, W);
+            const int wb = worker_of(fu + C.nb - 1, T, W);
+            bool write = wa == wb;
+            if (!write) {
+                const int slot = wid + u;
+                float4* part = p.partial + static_cast<size_t>(slot) * 8 * 32;
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) part[dt * 32 + lane] = make_float4(o[dt][0], o[dt][1], o[dt][2], o[dt][3]);
+                if (lane < 4) {
+                    float* ml = p.ml + static_cast<size_t>(slot) * 16;
+                    ml[2 * t] = m0;
+                    ml[2 * t + 1] = m1;
+                    ml[8 + 2 * t] = l0;
+                    ml[8 + 2 * t + 1] = l1;
+                }
+                __threadfence();
+                __syncwarp();
+                int old = 0;
+                if (lane == 0) old = atomicAdd(p.tickets + u, 1);
+                old = shfl(old, 0);
+                if (old == wb - wa) {
+                    // last contributor: merge every slot of this unit
+                    __threadfence();
+                    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+                    for (int w = wa; w <= wb; ++w) {
+                        const int sl = w + u;
+                        const float* ml = p.ml + static_cast<size_t>(sl) * 16;
+                        const float mi0 = __ldcg(ml + 2 * t), mi1 = __ldcg(ml + 2 * t + 1);
+                        const float li0 = __ldcg(ml + 8 + 2 * t), li1 = __ldcg(ml + 9 + 2 * t);
+                        const float n0 = fmaxf(M0, mi0), n1 = fmaxf(M1, mi1);
+                        const float a0 = exp2f(M0 - n0), a1 = exp2f(M1 - n1);
+                        const float b0 = exp2f(mi0 - n0), b1 = exp2f(mi1 - n1);
+                        M0 = n0;
+                        M1 = n1;
+                        L0 = L0 * a0 + li0 * b0;
+                        L1 = L1 * a1 + li1 * b1;
+                        const float4* part = p.partial + static_cast<size_t>(sl) * 8 * 32;
+#pragma unroll
+                        for (int dt = 0; dt < 8; ++dt) {
+                            const float4 v = __ldcg(part + dt * 32 + lane);
+                            o[dt][0] = o[dt][0] * a0 + v.x * b0;
+                            o[dt][1] = o[dt][1] * a1 + v.y * b1;
+                            o[dt][2] = o[dt][2] * a0 + v.z * b0;
+                            o[dt][3] = o[dt][3] * a1 + v.w * b1;
+                        }
+                    }
+                    l0 = L0;
+                    l1 = L1;
+                    write = true;
+                    if (lane == 0) p.tickets[u] = 0;
+                }
+            }
+            if (write) {
+                const int h = C.uh / p.head_groups;
+                const int hg = C.uh % p.head_groups;
+                const float inv0 = vscale / l0, inv1 = vscale / l1;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int gh = hg * kHeadsPerGroup + 2 * t + e;
+                    if (gh >= p.group) continue;
+                    const float inv = e ? inv1 : inv0;
+                    uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                                     (static_cast<size_t>(row_cur) * p.num_q_heads + h * p.group + gh) * kHeadDim;
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        const uint16_t lo = from_float<QBf16>(o[dt][e] * inv);
+                        const uint16_t hi = from_float<QBf16>(o[dt][2 + e] * inv);
+                        if constexpr (kFp8) {
+                            // rows g, g+8 of the tile are d = 16dt + 2g, 16dt + 2g + 1
+                            *reinterpret_cast<uint32_t*>(orow + 16 * dt + 2 * g) =
+                                static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+                        } else {
+                            orow[16 * dt + g] = lo;
+                            orow[16 * dt + g + 8] = hi;
+                        }
+                    }
+                }
+            }
+        }
+        cursor_advance(C, cum, B, UH);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+namespace {
+template <int Kind, bool QBf16>
+void* kernel_ptr() {
+    return reinterpret_cast<void*>(&decode_kernel<Kind, QBf16>);
+}
+
+void* decode_fn(CacheKind kind, bool q_bf16) {
+    switch (kind) {
+        case kKindBf16: return kernel_ptr<kKindBf16, true>();
+        case kKindFp16: return kernel_ptr<kKindFp16, false>();
+        case kKindFp8: return q_bf16 ? kernel_ptr<kKindFp8, true>() : kernel_ptr<kKindFp8, false>();
+    }
+    return nullptr;
+}
+
+int tile_area_bytes(CacheKind kind) {
+    switch (kind) {
+        case kKindBf16: return DecodeCfg<kKindBf16>::kTileArea + DecodeCfg<kKindBf16>::kBarBytes;
+        case kKindFp16: return DecodeCfg<kKindFp16>::kTileArea + DecodeCfg<kKindFp16>::kBarBytes;
+        case kKindFp8: return DecodeCfg<kKindFp8>::kTileArea + DecodeCfg<kKindFp8>::kBarBytes;
+    }
+    return 0;
+}
+}  // namespace
+
+size_t decode_smem_bytes(CacheKind kind, int num_seqs) {
+    // 1 KiB alignment slack + tiles + barriers + scan array
+    return 1024 + static_cast<size_t>(tile_area_bytes(kind)) + static_cast<size_t>(num_seqs + 1) * 4;
+}
+
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, size_t max_smem) {
+    return cudaFuncSetAttribute(decode_fn(kind, q_bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(max_smem));
+}
+
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_fn(kind, q_bf16),
+                                                         kDecodeWarps * 32, smem);
+}
+
+cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecodeWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    switch (kind) {
+        case kKindBf16: return cudaLaunchKernelEx(&cfg, decode_kernel<kKindBf16, true>, kmap, vmap, p);
+        case kKindFp16: return cudaLaunchKernelEx(&cfg, decode_kernel<kKindFp16, false>, kmap, vmap, p);
+        case kKindFp8:
+            return q_bf16 ? cudaLaunchKernelEx(&cfg, decode_kernel<kKindFp8, true>, kmap, vmap, p)
+                          : cudaLaunchKernelEx(&cfg, decode_kernel<kKindFp8, false>, kmap, vmap, p);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

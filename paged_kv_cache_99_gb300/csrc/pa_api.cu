@@ -1,0 +1,389 @@
+// C ABI of the paged attention library: argument checks, workspace layout,
+// tensor-map encoding and launches.  See include/pa.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    size_t max_smem_optin = 0;
+    bool decode_prepared[3][2] = {};
+    bool chunk_prepared[3][2] = {};
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+std::map<std::tuple<int, int, int, size_t>, int> g_occupancy;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// Device attributes of the current device; nullptr on failure.
+DeviceState* device_state(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_devices[dev];
+    if (!st.ready) {
+        int sms = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return nullptr;
+        st.sms = sms;
+        st.max_smem_optin = static_cast<size_t>(optin);
+        st.ready = true;
+    }
+    if (dev_out) *dev_out = dev;
+    return &st;
+}
+
+bool encode_fn() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+// Tensor map over a cache viewed as rows of 128 elements (one token of one KV
+// head); boxes of 16 rows, 128-byte swizzle.  16-bit caches are copied in two
+// 64-element halves, FP8 caches in one 128-byte box.
+pa_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads, bool fp8) {
+    if (!encode_fn()) return PA_ERR_CUDA;
+    const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * num_kv_heads * kBlockSize;
+    const cuuint64_t dims[2] = {kHeadDim, rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * (fp8 ? 1 : 2)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8 ? 128 : 64), kBlockSize};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int head_groups_of(int num_q_heads, int num_kv_heads) {
+    const int group = num_q_heads / num_kv_heads;
+    return (group + kHeadsPerGroup - 1) / kHeadsPerGroup;
+}
+
+int max_workers(const DeviceState& st) { return st.sms * kMaxDecodeCtasPerSm * kDecodeWarps; }
+
+// Checks shared by decode and mixed.
+pa_status check_attention_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                               const float* k_scale, const float* v_scale, const void* workspace) {
+    if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (q_dtype != PA_BF16 && q_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype != q_dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_seqs > kMaxSeqs) return PA_ERR_INVALID_ARG;
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace) return PA_ERR_INVALID_ARG;
+    if (cache_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(workspace, 256))
+        return PA_ERR_INVALID_ARG;
+    // tensor-map rows and flattened block counts must fit in 32 bits
+    const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * kBlockSize;
+    const long long units = static_cast<long long>(num_seqs) * num_kv_heads * head_groups_of(num_q_heads, num_kv_heads);
+    if (rows >= (1ll << 31) || units * max_blocks_per_seq >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+CacheKind kind_of(pa_dtype cache_dtype) {
+    return cache_dtype == PA_FP8_E4M3 ? kKindFp8 : (cache_dtype == PA_FP16 ? kKindFp16 : kKindBf16);
+}
+
+pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
+                      const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads, float scale,
+                      pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                      void* workspace, size_t workspace_bytes, int num_workers, int num_blocks,
+                      cudaStream_t stream) {
+    int dev = 0;
+    DeviceState* st = device_state(&dev);
+    if (!st) return PA_ERR_CUDA;
+    const CacheKind kind = kind_of(cache_dtype);
+    const bool q_bf16 = q_dtype == PA_BF16;
+    const size_t smem = decode_smem_bytes(kind, num_seqs);
+    if (smem > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
+    int ctas = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!st->decode_prepared[kind][q_bf16]) {
+            if (decode_prepare(kind, q_bf16, st->max_smem_optin) != cudaSuccess) return PA_ERR_CUDA;
+            st->decode_prepared[kind][q_bf16] = true;
+        }
+        auto key = std::make_tuple(dev, static_cast<int>(kind), static_cast<int>(q_bf16), smem);
+        auto it = g_occupancy.find(key);
+        if (it == g_occupancy.end()) {
+            if (decode_occupancy(kind, q_bf16, smem, &ctas) != cudaSuccess || ctas <= 0) return PA_ERR_CUDA;
+            g_occupancy[key] = ctas;
+        } else {
+            ctas = it->second;
+        }
+    }
+    ctas = ctas > kMaxDecodeCtasPerSm ? kMaxDecodeCtasPerSm : ctas;
+    const int full = st->sms * ctas * kDecodeWarps;
+    if (num_workers < 0 || num_workers > max_workers(*st)) return PA_ERR_INVALID_ARG;
+    const int W = num_workers == 0 ? full : num_workers;
+    const int hg = head_groups_of(num_q_heads, num_kv_heads);
+    const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_kv_heads, hg, W);
+    if (workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+
+    CUtensorMap kmap, vmap;
+    pa_status s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+    if (s != PA_OK) return s;
+    s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+    if (s != PA_OK) return s;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.query_start_loc = query_start_loc;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.status = reinterpret_cast<int*>(ws + lay.status_off);
+    p.tickets = reinterpret_cast<int*>(ws + lay.tickets_off);
+    p.ml = reinterpret_cast<float*>(ws + lay.ml_off);
+    p.partial = reinterpret_cast<float4*>(ws + lay.partial_off);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.head_groups = hg;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.num_workers = W;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = kDefaultTimeoutNs;
+    const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
+    return cuda_status(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream));
+}
+
+pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, const CUtensorMap& kmap,
+                     const CUtensorMap& vmap, const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* seq_lens, int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                     int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
+                     const float* v_scale, void* workspace, cudaStream_t stream) {
+    DeviceState* st = device_state(nullptr);
+    if (!st) return PA_ERR_CUDA;
+    const CacheKind kind = kind_of(cache_dtype);
+    const bool q_bf16 = q_dtype == PA_BF16;
+    const int group = num_q_heads / num_kv_heads;
+    const int qt = chunk_rows() / group;
+    if (qt < 1) return PA_ERR_UNSUPPORTED;
+    const size_t smem = chunk_smem_bytes(kind, num_seqs);
+    if (smem > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!st->chunk_prepared[kind][q_bf16]) {
+            if (chunk_prepare(kind, q_bf16, st->max_smem_optin) != cudaSuccess) return PA_ERR_CUDA;
+            st->chunk_prepared[kind][q_bf16] = true;
+        }
+    }
+    const long long grid_x = static_cast<long long>(num_seqs) + (total_q + qt - 1) / qt;
+    if (grid_x >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    ChunkParams p;
+    p.out = out;
+    p.q = q;
+    p.query_start_loc = query_start_loc;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.status = static_cast<int*>(workspace);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.queries_per_tile = qt;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = kDefaultTimeoutNs;
+    return cuda_status(launch_chunk(kind, q_bf16, kmap, vmap, p, static_cast<int>(grid_x), smem, stream));
+}
+
+}  // namespace
+
+WorkspaceLayout decode_workspace_layout(int num_seqs, int num_kv_heads, int head_groups, int workers) {
+    WorkspaceLayout l;
+    const size_t units = static_cast<size_t>(num_seqs) * num_kv_heads * head_groups;
+    const size_t slots = units + static_cast<size_t>(workers);
+    l.status_off = 0;
+    l.tickets_off = 256;
+    l.ml_off = l.tickets_off + round_up(units * 4, 256);
+    l.partial_off = l.ml_off + round_up(slots * 16 * 4, 256);
+    l.total = l.partial_off + slots * 8 * 32 * sizeof(float4);
+    return l;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported parameters";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_TIMEOUT: return "device wait timed out";
+        case PA_ERR_OUT_OF_RANGE: return "block-table entry outside the pool";
+        case PA_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+int pa_version(void) { return 100; }
+
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, pa_dtype src_dtype, pa_dtype cache_dtype,
+                               const float* k_scale, const float* v_scale, pa_stream_t stream) {
+    if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (src_dtype != PA_BF16 && src_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype != src_dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (cache_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    if (static_cast<long long>(num_tokens) * num_kv_heads >= (1ll << 34)) return PA_ERR_UNSUPPORTED;
+    return cuda_status(launch_reshape(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, num_blocks,
+                                      src_dtype == PA_BF16, cache_dtype == PA_FP8_E4M3, k_scale, v_scale,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+    if (num_seqs < 0 || num_seqs > kMaxSeqs || head_dim != kHeadDim || num_kv_heads <= 0 || num_q_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0)
+        return 0;
+    DeviceState* st = device_state(nullptr);
+    if (!st) return 0;
+    return decode_workspace_layout(num_seqs, num_kv_heads, head_groups_of(num_q_heads, num_kv_heads),
+                                   max_workers(*st))
+        .total;
+}
+
+int pa_default_workers(void) {
+    DeviceState* st = device_state(nullptr);
+    return st ? max_workers(*st) : 0;
+}
+
+pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       float scale, pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
+                       const float* v_scale, void* workspace, size_t workspace_bytes, int num_workers,
+                       pa_stream_t stream) {
+    pa_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                       scale, q_dtype, cache_dtype, k_scale, v_scale, workspace);
+    if (s != PA_OK) return s;
+    if (num_seqs == 0) return PA_OK;
+    return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                       num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
+                       workspace_bytes, num_workers, num_blocks, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                    pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return pa_decode_ex(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, q_dtype, cache_dtype,
+                        k_scale, v_scale, workspace, workspace_bytes, 0, stream);
+}
+
+pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
+                   const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                   int num_seqs, int total_q, int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                   const float* k_scale, const float* v_scale, void* workspace, size_t workspace_bytes,
+                   pa_stream_t stream) {
+    pa_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                       scale, q_dtype, cache_dtype, k_scale, v_scale, workspace);
+    if (s != PA_OK) return s;
+    if (!query_start_loc || total_q < 0 || max_q_len < 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (max_q_len >= 2) {
+        const CacheKind kind = kind_of(cache_dtype);
+        CUtensorMap kmap, vmap;
+        s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        if (s != PA_OK) return s;
+        s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        if (s != PA_OK) return s;
+        s = chunk_impl(out, q, query_start_loc, kmap, vmap, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                       total_q, num_q_heads, num_kv_heads, num_blocks, scale, q_dtype, cache_dtype, k_scale,
+                       v_scale, workspace, cs);
+        if (s != PA_OK) return s;
+    }
+    return decode_impl(out, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                       num_seqs, num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale,
+                       workspace, workspace_bytes, 0, num_blocks, cs);
+}
+
+pa_status pa_read_device_status(void* workspace, pa_stream_t stream) {
+    if (!workspace) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (word & kDevErrTimeout) return PA_ERR_TIMEOUT;
+    if (word & kDevErrRange) return PA_ERR_OUT_OF_RANGE;
+    return PA_OK;
+}
+
+pa_status pa_selftest_wait_timeout(void* workspace, size_t workspace_bytes, unsigned timeout_us,
+                                   pa_stream_t stream) {
+    if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+    if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return PA_ERR_INVALID_ARG;
+    return cuda_status(launch_wait_selftest(static_cast<int*>(workspace), 1000ull * timeout_us,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

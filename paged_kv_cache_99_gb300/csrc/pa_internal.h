@@ -1,0 +1,109 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+enum CacheKind { kKindBf16 = 0, kKindFp16 = 1, kKindFp8 = 2 };
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 16;
+constexpr int kMaxSeqs = 8192;
+constexpr int kDecodeWarps = 4;        // warps per decode CTA
+constexpr int kMaxDecodeCtasPerSm = 2;
+constexpr int kHeadsPerGroup = 8;      // query heads handled by one decode unit (MMA N)
+
+// Bits of the device-side status word (first word of the workspace).
+constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrRange = 2;
+
+// Decode: one "unit" = (sequence, KV head, group of up to 8 query heads).  The
+// cached blocks of all units are laid end to end and cut into equal ranges, one
+// per worker (warp).  A unit covered by several workers is merged through the
+// partial slots; slot (worker w, unit u) = w + u is unique because both indices
+// only grow along the flattened order.
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* query_start_loc;   // non-null: mixed batch, only rows with q_len == 1
+    const float* k_scale;
+    const float* v_scale;
+    int* status;                      // device status word
+    int* tickets;                     // [units], zero between calls
+    float* ml;                        // [slots][16]: running max (8 heads), sum (8 heads)
+    float4* partial;                  // [slots][8][32]: unnormalised output fragments
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                        // query heads per KV head
+    int head_groups;                  // ceil(group / 8)
+    int max_blocks;                   // block-table row length
+    int num_blocks;                   // pool size
+    int num_workers;                  // warps taking part
+    float scale_log2;                 // softmax scale * log2(e)
+    unsigned long long timeout_ns;    // bound of every barrier wait
+};
+
+// Prefill chunk tiles of a mixed batch (causal, no split).
+struct ChunkParams {
+    void* out;
+    const void* q;
+    const int32_t* query_start_loc;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const float* k_scale;
+    const float* v_scale;
+    int* status;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int max_blocks;
+    int num_blocks;
+    int queries_per_tile;             // queries of one sequence per CTA tile
+    float scale_log2;
+    unsigned long long timeout_ns;
+};
+
+struct WorkspaceLayout {
+    size_t status_off;
+    size_t tickets_off;
+    size_t ml_off;
+    size_t partial_off;
+    size_t total;
+};
+
+WorkspaceLayout decode_workspace_layout(int num_seqs, int num_kv_heads, int head_groups, int slots_workers);
+
+// Decode kernels: dynamic shared memory for num_seqs sequences.
+size_t decode_smem_bytes(CacheKind kind, int num_seqs);
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, size_t max_smem);
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas_per_sm);
+cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
+                          const CUtensorMap& vmap, const DecodeParams& p, int grid, size_t smem,
+                          cudaStream_t stream);
+
+// Slot write.
+cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,
+                           const int64_t* slots, int num_tokens, int num_kv_heads, int num_blocks,
+                           bool src_bf16, bool cache_fp8, const float* k_scale,
+                           const float* v_scale, cudaStream_t stream);
+
+// Prefill chunks.
+size_t chunk_smem_bytes(CacheKind kind, int num_seqs);
+int chunk_rows();
+cudaError_t chunk_prepare(CacheKind kind, bool q_bf16, size_t max_smem);
+cudaError_t launch_chunk(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
+                         const CUtensorMap& vmap, const ChunkParams& p, int grid_x, size_t smem,
+                         cudaStream_t stream);
+
+// Bounded-wait self test.
+cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,99 @@
+// Slot write ("reshape_and_cache") for sm_103a.
+//
+// Every new token's K and V vectors (one per KV head) go to the cache slot the
+// slot mapping names: physical block slot / 16, offset slot % 16 ("Basics of
+// LLM Inference and vLLM Internals", s.4: a block table maps logical blocks to
+// physical blocks; the slot mapping is that table resolved per token).
+//
+// One warp per (token, KV head): lanes 0-15 move the 256-byte K row, lanes
+// 16-31 the V row, 16 bytes per lane.  An FP8 cache stores
+// e4m3(fl32(x) / scale): IEEE division, then round-to-nearest-even to E4M3 with
+// saturation to +-448 (the hardware's satfinite conversion); NaN keeps its sign
+// as S.1111.111 and a result of magnitude zero keeps the sign of the quotient.
+#include <cuda_runtime.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+__device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
+    uint16_t y;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(y) : "f"(hi), "f"(lo));
+    uint32_t c_lo = y & 0xffu, c_hi = y >> 8;
+    const uint32_t s_lo = signbit(lo) ? 0x80u : 0u, s_hi = signbit(hi) ? 0x80u : 0u;
+    if (isnan(lo)) c_lo = s_lo | 0x7fu;
+    else if ((c_lo & 0x7fu) == 0) c_lo = s_lo;
+    if (isnan(hi)) c_hi = s_hi | 0x7fu;
+    else if ((c_hi & 0x7fu) == 0) c_hi = s_hi;
+    return c_lo | (c_hi << 8);
+}
+
+template <bool SrcBf16, bool Fp8>
+__global__ void __launch_bounds__(256)
+    reshape_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, void* k_cache,
+                   void* v_cache, const int64_t* __restrict__ slots, int num_tokens, int num_kv_heads,
+                   int num_blocks, const float* k_scale, const float* v_scale) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const long long pair = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (pair >= static_cast<long long>(num_tokens) * num_kv_heads) return;
+    const int tok = static_cast<int>(pair / num_kv_heads);
+    const int h = static_cast<int>(pair % num_kv_heads);
+    const long long slot = slots[tok];
+    if (slot < 0 || slot >= static_cast<long long>(num_blocks) * kBlockSize) return;
+    const int lane = threadIdx.x & 31;
+    const bool is_v = lane >= 16;
+    const int col = (lane & 15) * 8;
+    const uint16_t* src = (is_v ? v : k) + (static_cast<size_t>(tok) * num_kv_heads + h) * kHeadDim + col;
+    const size_t dst = ((static_cast<size_t>(slot >> 4) * num_kv_heads + h) * kBlockSize + (slot & 15)) * kHeadDim + col;
+    const uint4 x = *reinterpret_cast<const uint4*>(src);
+    if constexpr (!Fp8) {
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(is_v ? v_cache : k_cache) + dst) = x;
+    } else {
+        const float scale = __ldg(is_v ? v_scale : k_scale);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t out[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float a = __fdiv_rn(to_float<SrcBf16>(w[2 * i] & 0xffff), scale);
+            const float b = __fdiv_rn(to_float<SrcBf16>(w[2 * i] >> 16), scale);
+            const float c = __fdiv_rn(to_float<SrcBf16>(w[2 * i + 1] & 0xffff), scale);
+            const float d = __fdiv_rn(to_float<SrcBf16>(w[2 * i + 1] >> 16), scale);
+            out[i] = e4m3_pair(a, b) | (e4m3_pair(c, d) << 16);
+        }
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(is_v ? v_cache : k_cache) + dst) = make_uint2(out[0], out[1]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,
+                           const int64_t* slots, int num_tokens, int num_kv_heads, int num_blocks,
+                           bool src_bf16, bool cache_fp8, const float* k_scale,
+                           const float* v_scale, cudaStream_t stream) {
+    const long long pairs = static_cast<long long>(num_tokens) * num_kv_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((pairs + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint16_t* kk = static_cast<const uint16_t*>(k);
+    const uint16_t* vv = static_cast<const uint16_t*>(v);
+    if (cache_fp8) {
+        return src_bf16 ? cudaLaunchKernelEx(&cfg, reshape_kernel<true, true>, kk, vv, k_cache, v_cache, slots,
+                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale)
+                        : cudaLaunchKernelEx(&cfg, reshape_kernel<false, true>, kk, vv, k_cache, v_cache, slots,
+                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale);
+    }
+    return cudaLaunchKernelEx(&cfg, reshape_kernel<true, false>, kk, vv, k_cache, v_cache, slots, num_tokens,
+                              num_kv_heads, num_blocks, k_scale, v_scale);
+}
+
+}  // namespace pa
