@@ -73,6 +73,11 @@ PA_API const char* pa_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 PA_API int pa_version(void);
 
+/* Text of the last CUDA failure seen by a call of this thread that returned
+ * PA_ERR_CUDA (which CUDA call failed and its error string); "" if none.  The
+ * buffer is thread-local and valid until the next failing call. */
+PA_API const char* pa_last_error(void);
+
 /*
  * Slot write ("reshape_and_cache") [P1 s.4 block table; P3 "PagedAttention
  * changes the shape of the problem"].
@@ -90,8 +95,9 @@ PA_API int pa_version(void);
  *   cache_dtype    == src_dtype (bits copied unchanged), or PA_FP8_E4M3:
  *                  code = e4m3(fl32(x) / scale), the quotient rounded once to
  *                  binary32 (IEEE division), then round-to-nearest-even to E4M3 with
- *                  magnitudes above 448 clamped to 448; NaN -> S.1111.111 (sign
- *                  kept); -0 -> 0x80 [P1 s.2, s.7 "--kv-cache-dtype fp8"].
+ *                  magnitudes above 448 clamped to 448; a NaN quotient ->
+ *                  S.1111.111 with S the sign bit of the source element x; a zero
+ *                  result keeps the quotient's sign [P1 s.2, s.7 "--kv-cache-dtype fp8"].
  *   k_scale,v_scale device float32 scalars; required (non-NULL) iff FP8.
  * Bytes outside the written slots are never touched.
  */

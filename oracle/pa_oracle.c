@@ -137,6 +137,16 @@ uint8_t or_e4m3_encode(float x) {
     return (uint8_t)(sign | ((kv + 7) << 3) | mant);
 }
 
+/* The slot-write rule for one element: the quotient fl32(x) / scale (IEEE
+ * binary32 division), rounded to E4M3 as above.  A NaN quotient takes the sign
+ * of the source element x, so the code does not depend on how a platform
+ * propagates NaN signs through division (reading; the pages do not cover NaN). */
+uint8_t or_slot_code(float x, float scale) {
+    float q = x / scale;
+    if (isnan(q)) return (uint8_t)((signbit(x) ? 0x80 : 0x00) | 0x7F);
+    return or_e4m3_encode(q);
+}
+
 static double or_load(const void* base, int64_t idx, int dtype) {
     switch (dtype) {
         case OR_BF16: return or_bf16_to_double(((const uint16_t*)base)[idx]);
@@ -157,8 +167,8 @@ static double or_load(const void* base, int64_t idx, int dtype) {
  * Cache layout [num_blocks][num_kv_heads][block_size][head_dim]; a negative slot
  * is padding and writes nothing (readings; the pages do not fix either).
  * A 16-bit cache receives the source bits unchanged (source and cache type must
- * then agree).  An FP8 cache receives e4m3(fl32(x) / scale), the quotient
- * rounded once to binary32 (IEEE division), with separate K and V scales.
+ * then agree).  An FP8 cache receives or_slot_code(x, scale): e4m3(fl32(x) /
+ * scale), the quotient rounded once to binary32, with separate K and V scales.
  * All other cache bytes are left untouched.  Returns OR_ERR_RANGE if a slot
  * lies beyond the pool (nothing is written for that token).
  */
@@ -187,8 +197,8 @@ int or_reshape_and_cache(const uint16_t* k, const uint16_t* v, int src_dtype,
                 if (cache_dtype == OR_FP8_E4M3) {
                     float xk = (float)or_load(k, src, src_dtype);
                     float xv = (float)or_load(v, src, src_dtype);
-                    ((uint8_t*)k_cache)[dst] = or_e4m3_encode(xk / k_scale);
-                    ((uint8_t*)v_cache)[dst] = or_e4m3_encode(xv / v_scale);
+                    ((uint8_t*)k_cache)[dst] = or_slot_code(xk, k_scale);
+                    ((uint8_t*)v_cache)[dst] = or_slot_code(xv, v_scale);
                 } else {
                     ((uint16_t*)k_cache)[dst] = k[src];
                     ((uint16_t*)v_cache)[dst] = v[src];
@@ -384,7 +394,7 @@ void or_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
 void or_quantize_array(const uint16_t* x, int src_dtype, float scale, uint8_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) {
         float xf = (float)or_load(x, i, src_dtype);
-        out[i] = or_e4m3_encode(xf / scale);
+        out[i] = or_slot_code(xf, scale);
     }
 }
 

@@ -26,7 +26,10 @@ _DTYPE = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.uint8: PA_FP8_E
 class PagedAttentionError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {_lib().pa_status_string(status).decode()} (status {status})")
+        msg = f"{what}: {_lib().pa_status_string(status).decode()} (status {status})"
+        if status == PA_ERR_CUDA:
+            msg += f": {_lib().pa_last_error().decode()}"
+        super().__init__(msg)
 
 
 _LIB = None
@@ -50,6 +53,8 @@ def _lib():
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
     lib.pa_version.restype = I
+    lib.pa_last_error.argtypes = []
+    lib.pa_last_error.restype = ctypes.c_char_p
     lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
     lib.pa_reshape_and_cache.restype = I
     lib.pa_workspace_size.argtypes = [I, I, I, I]

@@ -164,7 +164,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
     grid_launch_dependents();
 
     const long long T = cum[B];
-    const int W = p.num_workers;
+    // never more workers than blocks, so that every worker's range is non-empty and
+    // the workers covering a unit are exactly worker_of(first) .. worker_of(last)
+    const int W = static_cast<int>(min(static_cast<long long>(p.num_workers), T));
     const int wid = blockIdx.x * kDecodeWarps + warp;
     if (wid >= W || T == 0) return;
     const long long f0 = T * wid / W;
@@ -537,8 +539,16 @@ size_t decode_smem_bytes(CacheKind kind, int num_seqs) {
 }
 
 cudaError_t decode_prepare(CacheKind kind, bool q_bf16, size_t max_smem) {
+    // the largest request a call can make (kMaxSeqs sequences), within what the
+    // device allows next to the kernel's static shared memory
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_fn(kind, q_bf16));
+    if (e != cudaSuccess) return e;
+    size_t want = decode_smem_bytes(kind, kMaxSeqs);
+    const size_t cap = max_smem > fa.sharedSizeBytes ? max_smem - fa.sharedSizeBytes : 0;
+    if (want > cap) want = cap;
     return cudaFuncSetAttribute(decode_fn(kind, q_bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(max_smem));
+                                static_cast<int>(want));
 }
 
 cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas_per_sm) {

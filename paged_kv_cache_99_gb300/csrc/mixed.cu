@@ -450,8 +450,14 @@ size_t chunk_smem_bytes(CacheKind kind, int num_seqs) {
 int chunk_rows() { return kChunkRows; }
 
 cudaError_t chunk_prepare(CacheKind kind, bool q_bf16, size_t max_smem) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, chunk_fn(kind, q_bf16));
+    if (e != cudaSuccess) return e;
+    size_t want = chunk_smem_bytes(kind, kMaxSeqs);
+    const size_t cap = max_smem > fa.sharedSizeBytes ? max_smem - fa.sharedSizeBytes : 0;
+    if (want > cap) want = cap;
     return cudaFuncSetAttribute(chunk_fn(kind, q_bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(max_smem));
+                                static_cast<int>(want));
 }
 
 cudaError_t launch_chunk(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdio>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -31,19 +32,37 @@ std::map<int, DeviceState> g_devices;
 std::map<std::tuple<int, int, int, size_t>, int> g_occupancy;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+thread_local char g_last_error[256] = "";
+
+pa_status fail(const char* what, cudaError_t e) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
+    return PA_ERR_CUDA;
+}
+
+pa_status fail_msg(const char* what) {
+    snprintf(g_last_error, sizeof g_last_error, "%s", what);
+    return PA_ERR_CUDA;
+}
+
+pa_status cuda_status(cudaError_t e, const char* what) { return e == cudaSuccess ? PA_OK : fail(what, e); }
 
 // Device attributes of the current device; nullptr on failure.
 DeviceState* device_state(int* dev_out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        fail("cudaGetDevice", e);
+        return nullptr;
+    }
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState& st = g_devices[dev];
     if (!st.ready) {
         int sms = 0, optin = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
-        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) {
+            fail("cudaDeviceGetAttribute", e);
             return nullptr;
+        }
         st.sms = sms;
         st.max_smem_optin = static_cast<size_t>(optin);
         st.ready = true;
@@ -56,11 +75,13 @@ bool encode_fn() {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_encode) return true;
     void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || fn == nullptr)
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        snprintf(g_last_error, sizeof g_last_error, "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled): %s, query %d",
+                 cudaGetErrorString(e), static_cast<int>(q));
         return false;
+    }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     return true;
 }
@@ -79,7 +100,11 @@ pa_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, i
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -134,18 +159,21 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     const CacheKind kind = kind_of(cache_dtype);
     const bool q_bf16 = q_dtype == PA_BF16;
     const size_t smem = decode_smem_bytes(kind, num_seqs);
-    if (smem > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
+    if (smem + 1024 > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
     int ctas = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!st->decode_prepared[kind][q_bf16]) {
-            if (decode_prepare(kind, q_bf16, st->max_smem_optin) != cudaSuccess) return PA_ERR_CUDA;
+            cudaError_t e = decode_prepare(kind, q_bf16, st->max_smem_optin);
+            if (e != cudaSuccess) return fail("cudaFuncSetAttribute(decode)", e);
             st->decode_prepared[kind][q_bf16] = true;
         }
         auto key = std::make_tuple(dev, static_cast<int>(kind), static_cast<int>(q_bf16), smem);
         auto it = g_occupancy.find(key);
         if (it == g_occupancy.end()) {
-            if (decode_occupancy(kind, q_bf16, smem, &ctas) != cudaSuccess || ctas <= 0) return PA_ERR_CUDA;
+            cudaError_t e = decode_occupancy(kind, q_bf16, smem, &ctas);
+            if (e != cudaSuccess) return fail("cudaOccupancyMaxActiveBlocksPerMultiprocessor(decode)", e);
+            if (ctas <= 0) return fail_msg("decode kernel does not fit on an SM");
             g_occupancy[key] = ctas;
         } else {
             ctas = it->second;
@@ -189,7 +217,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
-    return cuda_status(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream));
+    return cuda_status(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream), "launch(decode)");
 }
 
 pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, const CUtensorMap& kmap,
@@ -205,11 +233,12 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     const int qt = chunk_rows() / group;
     if (qt < 1) return PA_ERR_UNSUPPORTED;
     const size_t smem = chunk_smem_bytes(kind, num_seqs);
-    if (smem > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
+    if (smem + 1024 > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!st->chunk_prepared[kind][q_bf16]) {
-            if (chunk_prepare(kind, q_bf16, st->max_smem_optin) != cudaSuccess) return PA_ERR_CUDA;
+            cudaError_t e = chunk_prepare(kind, q_bf16, st->max_smem_optin);
+            if (e != cudaSuccess) return fail("cudaFuncSetAttribute(chunk)", e);
             st->chunk_prepared[kind][q_bf16] = true;
         }
     }
@@ -233,7 +262,8 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.queries_per_tile = qt;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
-    return cuda_status(launch_chunk(kind, q_bf16, kmap, vmap, p, static_cast<int>(grid_x), smem, stream));
+    return cuda_status(launch_chunk(kind, q_bf16, kmap, vmap, p, static_cast<int>(grid_x), smem, stream),
+                       "launch(chunk)");
 }
 
 }  // namespace
@@ -271,6 +301,8 @@ const char* pa_status_string(int status) {
 
 int pa_version(void) { return 100; }
 
+const char* pa_last_error(void) { return g_last_error; }
+
 pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
                                int block_size, int num_blocks, pa_dtype src_dtype, pa_dtype cache_dtype,
@@ -288,7 +320,8 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
     if (static_cast<long long>(num_tokens) * num_kv_heads >= (1ll << 34)) return PA_ERR_UNSUPPORTED;
     return cuda_status(launch_reshape(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, num_blocks,
                                       src_dtype == PA_BF16, cache_dtype == PA_FP8_E4M3, k_scale, v_scale,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+                                      reinterpret_cast<cudaStream_t>(stream)),
+                       "launch(reshape_and_cache)");
 }
 
 size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
@@ -367,11 +400,13 @@ pa_status pa_read_device_status(void* workspace, pa_stream_t stream) {
     if (!workspace) return PA_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int word = 0;
-    if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PA_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return fail("cudaMemcpyAsync(status)", e);
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail("cudaStreamSynchronize", e);
     if (word != 0) {
-        if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return PA_ERR_CUDA;
-        if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+        if ((e = cudaMemsetAsync(workspace, 0, sizeof(int), s)) != cudaSuccess) return fail("cudaMemsetAsync", e);
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail("cudaStreamSynchronize", e);
     }
     if (word & kDevErrTimeout) return PA_ERR_TIMEOUT;
     if (word & kDevErrRange) return PA_ERR_OUT_OF_RANGE;
@@ -383,7 +418,8 @@ pa_status pa_selftest_wait_timeout(void* workspace, size_t workspace_bytes, unsi
     if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
     if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return PA_ERR_INVALID_ARG;
     return cuda_status(launch_wait_selftest(static_cast<int*>(workspace), 1000ull * timeout_us,
-                                            reinterpret_cast<cudaStream_t>(stream)));
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                       "launch(reshape_and_cache)");
 }
 
 }  // extern "C"

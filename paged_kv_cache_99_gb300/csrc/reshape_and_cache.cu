@@ -8,8 +8,9 @@
 // One warp per (token, KV head): lanes 0-15 move the 256-byte K row, lanes
 // 16-31 the V row, 16 bytes per lane.  An FP8 cache stores
 // e4m3(fl32(x) / scale): IEEE division, then round-to-nearest-even to E4M3 with
-// saturation to +-448 (the hardware's satfinite conversion); NaN keeps its sign
-// as S.1111.111 and a result of magnitude zero keeps the sign of the quotient.
+// saturation to +-448 (the hardware's satfinite conversion); a NaN quotient
+// becomes S.1111.111 with the sign of the source element, and a result of
+// magnitude zero keeps the sign of the quotient.
 #include <cuda_runtime.h>
 
 #include "pa_device.cuh"
@@ -19,15 +20,21 @@ namespace pa {
 
 namespace {
 
-__device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
+// Codes of the two 16-bit source elements packed in `word` (low half first):
+// e4m3(fl32(x) / scale) with satfinite rounding; a NaN quotient takes the sign
+// bit of its source element (read from the raw bits: the fp16 -> fp32
+// conversion does not keep NaN signs), a zero code the sign of the quotient.
+template <bool SrcBf16>
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t word, float scale) {
+    const float lo = __fdiv_rn(to_float<SrcBf16>(word & 0xffffu), scale);
+    const float hi = __fdiv_rn(to_float<SrcBf16>(word >> 16), scale);
     uint16_t y;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(y) : "f"(hi), "f"(lo));
     uint32_t c_lo = y & 0xffu, c_hi = y >> 8;
-    const uint32_t s_lo = signbit(lo) ? 0x80u : 0u, s_hi = signbit(hi) ? 0x80u : 0u;
-    if (isnan(lo)) c_lo = s_lo | 0x7fu;
-    else if ((c_lo & 0x7fu) == 0) c_lo = s_lo;
-    if (isnan(hi)) c_hi = s_hi | 0x7fu;
-    else if ((c_hi & 0x7fu) == 0) c_hi = s_hi;
+    if (isnan(lo)) c_lo = ((word >> 8) & 0x80u) | 0x7fu;
+    else if ((c_lo & 0x7fu) == 0) c_lo = signbit(lo) ? 0x80u : 0u;
+    if (isnan(hi)) c_hi = ((word >> 24) & 0x80u) | 0x7fu;
+    else if ((c_hi & 0x7fu) == 0) c_hi = signbit(hi) ? 0x80u : 0u;
     return c_lo | (c_hi << 8);
 }
 
@@ -57,13 +64,8 @@ __global__ void __launch_bounds__(256)
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t out[2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float a = __fdiv_rn(to_float<SrcBf16>(w[2 * i] & 0xffff), scale);
-            const float b = __fdiv_rn(to_float<SrcBf16>(w[2 * i] >> 16), scale);
-            const float c = __fdiv_rn(to_float<SrcBf16>(w[2 * i + 1] & 0xffff), scale);
-            const float d = __fdiv_rn(to_float<SrcBf16>(w[2 * i + 1] >> 16), scale);
-            out[i] = e4m3_pair(a, b) | (e4m3_pair(c, d) << 16);
-        }
+        for (int i = 0; i < 2; ++i)
+            out[i] = e4m3_pair<SrcBf16>(w[2 * i], scale) | (e4m3_pair<SrcBf16>(w[2 * i + 1], scale) << 16);
         *reinterpret_cast<uint2*>(static_cast<uint8_t*>(is_v ? v_cache : k_cache) + dst) = make_uint2(out[0], out[1]);
     }
 }

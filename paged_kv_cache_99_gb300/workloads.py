@@ -71,6 +71,7 @@ class Workload:
     scale: float = 1.0 / math.sqrt(HEAD_DIM)
     seed: int = 0
     shared_prefix_blocks: int = 0
+    q_lens_host: list = field(default_factory=list)   # host copy: no device sync when read
 
     @property
     def total_q(self) -> int:
@@ -82,8 +83,7 @@ class Workload:
 
     @property
     def q_lens(self) -> list:
-        qsl = self.query_start_loc.tolist()
-        return [qsl[i + 1] - qsl[i] for i in range(self.num_seqs)]
+        return list(self.q_lens_host)
 
     @property
     def max_q_len(self) -> int:
@@ -220,7 +220,7 @@ def build_workload(*, name: str, seed: int, device, num_layers: int, seq_lens, q
         k_cache=k_cache, v_cache=v_cache,
         k_scale=torch.stack(k_scales).float() if k_scales else None,
         v_scale=torch.stack(v_scales).float() if v_scales else None,
-        seed=seed, shared_prefix_blocks=P)
+        seed=seed, shared_prefix_blocks=P, q_lens_host=list(q_lens))
 
 
 def _poison(cache: torch.Tensor, dtype: str, slots: torch.Tensor, free_blocks: torch.Tensor,

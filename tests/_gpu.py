@@ -93,7 +93,56 @@ def compare(gpu_out: torch.Tensor, rows, ref: np.ndarray, what: str = ""):
     bad = err > ATOL + RTOL * np.abs(ref)
     assert not bad.any(), f"{what}: {int(bad.sum())} elements outside tolerance, max err {err.max():.3e}"
     rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
-    # bf16 rounding of the probabilities and of the output is ~2^-9 relative; 1e-2 of the
-    # output RMS is far above that and catches dropped or doubled blocks the loose bound would miss
-    assert err.max(initial=0.0) <= 1e-2 * rms + 1e-3, f"{what}: max err {err.max():.3e} vs rms {rms:.3e}"
+    # rounding of the probabilities and of the output is ~2^-9 relative per element; the
+    # absolute term 1e-2 * rms (instead of 1e-2) still catches dropped or doubled blocks
+    # when outputs are small, where the stated bound alone would not
+    guard = err <= 1e-2 * np.abs(ref) + 1e-2 * rms
+    assert guard.all(), f"{what}: max err {err.max():.3e} vs rms {rms:.3e}"
     return float(err.max(initial=0.0)), rms
+
+
+def oracle_rows(w: W.Workload, layer: int, seqs, rows_per_seq: int = 6, seed: int = 0):
+    """Oracle outputs for a sample of query rows of the chosen sequences.
+
+    The oracle slot write is applied to the chosen sequences' new tokens; every
+    sampled row (always the first and last of its sequence) is then the oracle
+    decode of that one query over its causal prefix of pos + 1 tokens, which
+    the oracle tests show equals the mixed-batch row exactly.
+    """
+    rng = np.random.default_rng(seed)
+    qsl = w.query_start_loc.cpu().numpy()
+    lens = w.seq_lens.cpu().numpy()
+    tables = w.block_tables.cpu().numpy()
+    need = sorted({int(x) for s in seqs for x in tables[s, :-(-int(lens[s]) // w.block_size)]})
+    remap = {b: i for i, b in enumerate(need)}
+    idx = torch.tensor(need, dtype=torch.int64, device=w.k_cache[layer].device)
+    kc = raw(w.k_cache[layer].index_select(0, idx))
+    vc = raw(w.v_cache[layer].index_select(0, idx))
+    ks = float(w.k_scale[layer]) if w.k_scale is not None else 1.0
+    vs = float(w.v_scale[layer]) if w.v_scale is not None else 1.0
+    cd = CODE[w.cache_dtype]
+    if w.num_new_tokens:
+        slots = w.slot_mapping.cpu().numpy()
+        toks = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in seqs])
+        new_slots = np.array([remap[int(slots[r]) // w.block_size] * w.block_size + int(slots[r]) % w.block_size
+                              for r in toks], np.int64)
+        tsel = torch.as_tensor(toks, device=w.k_new.device)
+        kc, vc = oracle.reshape_and_cache(raw(w.k_new[layer][tsel]), raw(w.v_new[layer][tsel]), CODE[w.q_dtype],
+                                          kc, vc, cd, new_slots, ks, vs)
+    rows, outs = [], []
+    for s in seqs:
+        ql, n = int(qsl[s + 1] - qsl[s]), int(lens[s])
+        if ql == 0:
+            continue
+        js = sorted({0, ql - 1} | set(rng.choice(ql, min(ql, rows_per_seq), replace=False).tolist()))
+        nb = -(-n // w.block_size)
+        table = np.full((1, tables.shape[1]), -1, np.int32)
+        table[0, :nb] = [remap[int(x)] for x in tables[s, :nb]]
+        for j in js:
+            r = int(qsl[s]) + j
+            qb = raw(w.q[layer][r:r + 1])
+            o = oracle.decode(qb, CODE[w.q_dtype], kc, vc, cd, table, np.array([n - ql + j + 1], np.int32),
+                              w.scale, ks, vs)
+            rows.append(r)
+            outs.append(o[0])
+    return np.array(rows, np.int64), np.stack(outs)

@@ -1,0 +1,63 @@
+"""Host-side pieces of the benchmark, on CPU: the algorithmic byte count, the
+max-over-ranks timing reduction across two gloo ranks, and the oracle arm."""
+import json
+import os
+import socket
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from paged_kv_cache_99_gb300 import workloads as W
+
+
+def test_kv_bytes_tiny_and_per_token():
+    w = W.tiny("cpu")
+    assert bench.kv_read_bytes(w) == (8 + 17 + 31 + 46) * 2 * 2 * 128 * 2
+    # Qwen2.5-1.5B shape: 28 layers x 1,024 B = 28,672 B per token, as the sizing formula gives
+    w2 = W.qwen25_15b("cpu", num_layers=28, batch=2)
+    assert bench.kv_read_bytes(w2) == int(w2.seq_lens.sum()) * 28672
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.reduce_max(1.5 + rank, world)
+        bench.barrier(world)
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(60)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=5) for _ in range(2))
+    assert res == {0: 2.5, 1: 2.5}
+
+
+def test_reference_arm_prints_contract_line(capsys):
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3",
+                "--ref-step-seconds", "0.01"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
