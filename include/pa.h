@@ -110,12 +110,11 @@ PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cach
 /*
  * Bytes of workspace pa_decode / pa_mixed need on the CURRENT device for
  * num_seqs sequences (the default worker count depends on the device's SM
- * count).  The workspace is caller-owned device memory, 256-byte aligned, that
- * must be ZERO-FILLED once after allocation; every call that returns PA_OK and
- * completes on the device leaves it in that state again (apart from the status
- * word, see pa_read_device_status).  After a device-side PA_ERR_TIMEOUT, zero it
- * again.  One workspace must not be used by two calls that may overlap on the
- * GPU.  Returns 0 for invalid arguments.
+ * count).  The workspace is caller-owned device memory, 256-byte aligned; its
+ * contents need no initialisation (the first word is the device status word,
+ * see pa_read_device_status; the rest is scratch each call overwrites before
+ * reading).  One workspace must not be used by two calls that may overlap on
+ * the GPU.  Returns 0 for invalid arguments.
  */
 PA_API size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
 
@@ -146,8 +145,9 @@ PA_API int pa_default_workers(void);
  *                  is code * scale)
  *   workspace      see pa_workspace_size
  * num_seqs <= 8192.  The work is split evenly over the workers by cached
- * blocks (long sequences are split across workers and merged with a
- * log-sum-exp combine), so the result does not depend on where blocks live.
+ * blocks; a sequence split across workers is merged by a log-sum-exp combine
+ * launched behind the decode kernel on the same stream.  The result does not
+ * depend on where blocks live.
  */
 PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,

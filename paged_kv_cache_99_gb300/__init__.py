@@ -115,7 +115,7 @@ def pa_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_d
 
 
 def new_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, device=None) -> torch.Tensor:
-    """Zero-filled workspace of pa_workspace_size bytes on the current device."""
+    """Workspace of pa_workspace_size bytes (zeroed, so the status word starts clear)."""
     n = pa_workspace_size(num_seqs, num_q_heads, num_kv_heads)
     if n == 0:
         raise ValueError("invalid workspace arguments")

@@ -10,8 +10,11 @@
 //  * Work unit = (sequence, KV head, group of <= 8 query heads).  The cached
 //    blocks of all units are laid end to end and cut into equal contiguous
 //    ranges, one per warp, so every warp streams the same number of 4 KiB tiles
-//    whatever the length mix; a unit cut by a range boundary is merged by a
-//    log-sum-exp combine done by whichever warp finishes the unit last (ticket).
+//    whatever the length mix.  A unit a single warp covers is written directly;
+//    a unit cut by range boundaries leaves one partial (unnormalised output,
+//    running max and sum) per warp, merged by a log-sum-exp combine kernel
+//    chained behind by programmatic dependent launch, so no streaming warp ever
+//    waits on another.
 //  * Each warp owns a ring of stages in shared memory.  One lane issues bulk
 //    tensor copies (TMA, 128-byte swizzle) of the K and V tiles of a physical
 //    block straight from the block table; the ring keeps several tiles per warp
@@ -162,6 +165,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
     }
     __syncthreads();
     grid_launch_dependents();
+    if (blockIdx.x == 0) {
+        // the block prefix and worker count, for the combine kernel
+        for (int i = threadIdx.x; i <= B; i += blockDim.x) p.plan[i] = cum[i];
+        if (threadIdx.x == 0) p.plan[B + 1] = static_cast<int>(min(static_cast<long long>(p.num_workers), static_cast<long long>(cum[B])));
+    }
 
     const long long T = cum[B];
     // never more workers than blocks, so that every worker's range is non-empty and
@@ -419,10 +427,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
             }
             const int u = C.s * UH + C.uh;
             const long long fu = cum[C.s] + static_cast<long long>(C.uh) * C.nb;
-            const int wa = worker_of(fu, T, W);
-            const int wb = worker_of(fu + C.nb - 1, T, W);
-            bool write = wa == wb;
+            const bool write = worker_of(fu, T, W) == worker_of(fu + C.nb - 1, T, W);
             if (!write) {
+                // unit shared with other workers: plain partial store, merged by combine_kernel
                 const int slot = wid + u;
                 float4* part = p.partial + static_cast<size_t>(slot) * 8 * 32;
 #pragma unroll
@@ -433,44 +440,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
                     ml[2 * t + 1] = m1;
                     ml[8 + 2 * t] = l0;
                     ml[8 + 2 * t + 1] = l1;
-                }
-                __threadfence();
-                __syncwarp();
-                int old = 0;
-                if (lane == 0) old = atomicAdd(p.tickets + u, 1);
-                old = shfl(old, 0);
-                if (old == wb - wa) {
-                    // last contributor: merge every slot of this unit
-                    __threadfence();
-                    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-#pragma unroll
-                    for (int dt = 0; dt < 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-                    for (int w = wa; w <= wb; ++w) {
-                        const int sl = w + u;
-                        const float* ml = p.ml + static_cast<size_t>(sl) * 16;
-                        const float mi0 = __ldcg(ml + 2 * t), mi1 = __ldcg(ml + 2 * t + 1);
-                        const float li0 = __ldcg(ml + 8 + 2 * t), li1 = __ldcg(ml + 9 + 2 * t);
-                        const float n0 = fmaxf(M0, mi0), n1 = fmaxf(M1, mi1);
-                        const float a0 = exp2f(M0 - n0), a1 = exp2f(M1 - n1);
-                        const float b0 = exp2f(mi0 - n0), b1 = exp2f(mi1 - n1);
-                        M0 = n0;
-                        M1 = n1;
-                        L0 = L0 * a0 + li0 * b0;
-                        L1 = L1 * a1 + li1 * b1;
-                        const float4* part = p.partial + static_cast<size_t>(sl) * 8 * 32;
-#pragma unroll
-                        for (int dt = 0; dt < 8; ++dt) {
-                            const float4 v = __ldcg(part + dt * 32 + lane);
-                            o[dt][0] = o[dt][0] * a0 + v.x * b0;
-                            o[dt][1] = o[dt][1] * a1 + v.y * b1;
-                            o[dt][2] = o[dt][2] * a0 + v.z * b0;
-                            o[dt][3] = o[dt][3] * a1 + v.w * b1;
-                        }
-                    }
-                    l0 = L0;
-                    l1 = L1;
-                    write = true;
-                    if (lane == 0) p.tickets[u] = 0;
                 }
             }
             if (write) {
@@ -501,6 +470,114 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
             }
         }
         cursor_advance(C, cum, B, UH);
+    }
+}
+
+// Log-sum-exp combine of the units split across workers:
+//   out = sum_i e^{m_i - M} o_i / sum_i e^{m_i - M} l_i,   M = max_i m_i,
+// where worker i left its unnormalised output o_i, running max m_i (log2 units)
+// and running sum l_i.  One CTA per unit, one warp per 16-wide slice of d.
+// Pass 1 reads every slot's (m, l) with lanes in parallel and reduces over the
+// warp; pass 2 reads up to 16 slots' fragments per round trip.
+template <bool OutBf16, bool Fp8Layout>
+__global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
+    grid_dependency_wait();
+    const int UH = p.num_kv_heads * p.head_groups;
+    const int u = blockIdx.x;
+    const int s = u / UH, uh = u % UH;
+    const int B = p.num_seqs;
+    const int lo = p.plan[s], hi = p.plan[s + 1];
+    const int W = p.plan[B + 1];
+    const long long T = p.plan[B];
+    if (hi == lo || W <= 0) return;
+    const int nb = (hi - lo) / UH;
+    const long long fu = lo + static_cast<long long>(uh) * nb;
+    const int wa = worker_of(fu, T, W), wb = worker_of(fu + nb - 1, T, W);
+    if (wa == wb) return;   // its only worker wrote the output
+    const int nseg = wb - wa + 1;
+    const int dt = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
+
+    float Mh[8], Lh[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+        Mh[h] = -INFINITY;
+        Lh[h] = 0.f;
+    }
+    for (int base = 0; base < nseg; base += 32) {
+        const bool live = base + lane < nseg;
+        float mv[8], lv[8];
+        if (live) {
+            const float4* ml4 = reinterpret_cast<const float4*>(p.ml + static_cast<size_t>(wa + base + lane + u) * 16);
+            const float4 a = __ldcg(ml4), b = __ldcg(ml4 + 1), c = __ldcg(ml4 + 2), d = __ldcg(ml4 + 3);
+            mv[0] = a.x; mv[1] = a.y; mv[2] = a.z; mv[3] = a.w; mv[4] = b.x; mv[5] = b.y; mv[6] = b.z; mv[7] = b.w;
+            lv[0] = c.x; lv[1] = c.y; lv[2] = c.z; lv[3] = c.w; lv[4] = d.x; lv[5] = d.y; lv[6] = d.z; lv[7] = d.w;
+        } else {
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                mv[h] = -INFINITY;
+                lv[h] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            float mx = mv[h];
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+            const float nm = fmaxf(Mh[h], mx);
+            float c = live ? lv[h] * exp2f(mv[h] - nm) : 0.f;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) c += __shfl_xor_sync(0xffffffffu, c, o2);
+            Lh[h] = Lh[h] * exp2f(Mh[h] - nm) + c;
+            Mh[h] = nm;
+        }
+    }
+    const float M0 = t == 0 ? Mh[0] : t == 1 ? Mh[2] : t == 2 ? Mh[4] : Mh[6];
+    const float M1 = t == 0 ? Mh[1] : t == 1 ? Mh[3] : t == 2 ? Mh[5] : Mh[7];
+    const float L0 = t == 0 ? Lh[0] : t == 1 ? Lh[2] : t == 2 ? Lh[4] : Lh[6];
+    const float L1 = t == 0 ? Lh[1] : t == 1 ? Lh[3] : t == 2 ? Lh[5] : Lh[7];
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int base = 0; base < nseg; base += 16) {
+        float4 v[16];
+        float m0v[16], m1v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int sl = wa + min(base + k, nseg - 1) + u;
+            v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
+            m0v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t);
+            m1v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t + 1);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (base + k < nseg) {
+                const float w0 = exp2f(m0v[k] - M0), w1 = exp2f(m1v[k] - M1);
+                acc[0] += v[k].x * w0;
+                acc[1] += v[k].y * w1;
+                acc[2] += v[k].z * w0;
+                acc[3] += v[k].w * w1;
+            }
+        }
+    }
+    const float vscale = Fp8Layout ? __ldg(p.v_scale) : 1.0f;
+    const int h = uh / p.head_groups;
+    const int hg = uh % p.head_groups;
+    const int row = p.query_start_loc ? p.query_start_loc[s] : s;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int gh = hg * kHeadsPerGroup + 2 * t + e;
+        if (gh >= p.group) continue;
+        const float inv = vscale / (e ? L1 : L0);
+        uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                         (static_cast<size_t>(row) * p.num_q_heads + h * p.group + gh) * kHeadDim;
+        const uint16_t lo16 = from_float<OutBf16>(acc[e] * inv);
+        const uint16_t hi16 = from_float<OutBf16>(acc[2 + e] * inv);
+        if constexpr (Fp8Layout) {
+            *reinterpret_cast<uint32_t*>(orow + 16 * dt + 2 * g) =
+                static_cast<uint32_t>(lo16) | (static_cast<uint32_t>(hi16) << 16);
+        } else {
+            orow[16 * dt + g] = lo16;
+            orow[16 * dt + g + 8] = hi16;
+        }
     }
 }
 
@@ -576,6 +653,24 @@ cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, 
                           : cudaLaunchKernelEx(&cfg, decode_kernel<kKindFp8, false>, kmap, vmap, p);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, cudaStream_t stream) {
+    const long long units = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.head_groups;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (fp8_cache)
+        return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, true>, p)
+                        : cudaLaunchKernelEx(&cfg, combine_kernel<false, true>, p);
+    return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, false>, p)
+                    : cudaLaunchKernelEx(&cfg, combine_kernel<false, false>, p);
 }
 
 }  // namespace pa

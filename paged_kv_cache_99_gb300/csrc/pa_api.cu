@@ -203,7 +203,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.status = reinterpret_cast<int*>(ws + lay.status_off);
-    p.tickets = reinterpret_cast<int*>(ws + lay.tickets_off);
+    p.plan = reinterpret_cast<int*>(ws + lay.plan_off);
     p.ml = reinterpret_cast<float*>(ws + lay.ml_off);
     p.partial = reinterpret_cast<float4*>(ws + lay.partial_off);
     p.num_seqs = num_seqs;
@@ -217,7 +217,9 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
-    return cuda_status(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream), "launch(decode)");
+    s = cuda_status(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream), "launch(decode)");
+    if (s != PA_OK) return s;
+    return cuda_status(launch_combine(q_bf16, kind == kKindFp8, p, stream), "launch(combine)");
 }
 
 pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, const CUtensorMap& kmap,
@@ -273,8 +275,8 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_kv_heads, int head
     const size_t units = static_cast<size_t>(num_seqs) * num_kv_heads * head_groups;
     const size_t slots = units + static_cast<size_t>(workers);
     l.status_off = 0;
-    l.tickets_off = 256;
-    l.ml_off = l.tickets_off + round_up(units * 4, 256);
+    l.plan_off = 256;
+    l.ml_off = l.plan_off + round_up((static_cast<size_t>(num_seqs) + 2) * 4, 256);
     l.partial_off = l.ml_off + round_up(slots * 16 * 4, 256);
     l.total = l.partial_off + slots * 8 * 32 * sizeof(float4);
     return l;

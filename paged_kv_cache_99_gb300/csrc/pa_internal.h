@@ -23,9 +23,9 @@ constexpr int kDevErrRange = 2;
 
 // Decode: one "unit" = (sequence, KV head, group of up to 8 query heads).  The
 // cached blocks of all units are laid end to end and cut into equal ranges, one
-// per worker (warp).  A unit covered by several workers is merged through the
-// partial slots; slot (worker w, unit u) = w + u is unique because both indices
-// only grow along the flattened order.
+// per worker (warp).  A unit covered by several workers leaves partials in the
+// slots (worker w, unit u) -> w + u, unique because both indices only grow
+// along the flattened order; the combine kernel merges them.
 struct DecodeParams {
     void* out;
     const void* q;
@@ -35,7 +35,7 @@ struct DecodeParams {
     const float* k_scale;
     const float* v_scale;
     int* status;                      // device status word
-    int* tickets;                     // [units], zero between calls
+    int* plan;                        // [num_seqs + 2]: block prefix per sequence, then workers used
     float* ml;                        // [slots][16]: running max (8 heads), sum (8 heads)
     float4* partial;                  // [slots][8][32]: unnormalised output fragments
     int num_seqs;
@@ -73,7 +73,7 @@ struct ChunkParams {
 
 struct WorkspaceLayout {
     size_t status_off;
-    size_t tickets_off;
+    size_t plan_off;
     size_t ml_off;
     size_t partial_off;
     size_t total;
@@ -88,6 +88,7 @@ cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas
 cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, const DecodeParams& p, int grid, size_t smem,
                           cudaStream_t stream);
+cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, cudaStream_t stream);
 
 // Slot write.
 cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,

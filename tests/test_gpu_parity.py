@@ -211,15 +211,14 @@ def test_bounded_wait_times_out_and_context_survives():
     compare(out, rows, ref, "after timeout")
 
 
-def test_workspace_stays_zero_between_calls():
+def test_workspace_needs_no_initialisation():
     w = _case(39, [3000, 10, 700], 8, write_new=False)
     ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads)
-    for _ in range(3):
+    for fill in (0xFF, 0x7F, 0x00):
+        ws[256:].fill_(fill)          # scratch holds garbage (NaN patterns for 0xFF / 0x7F)
         out, _, _ = gpu_step(w, workspace=ws, num_workers=40)
-    ntick = w.num_seqs * w.num_kv_heads
-    assert torch.count_nonzero(ws[256:256 + 4 * ntick]) == 0
-    rows, ref = oracle_step(w)
-    compare(out, rows, ref, "repeated")
+        rows, ref = oracle_step(w)
+        compare(out, rows, ref, f"scratch filled with {fill:#x}")
 
 
 # ---------------------------------------------------------------- mixed batch
