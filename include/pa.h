@@ -193,6 +193,40 @@ PA_API pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_l
                    pa_stream_t stream);
 
 /*
+ * Decode without a caller-provided workspace (no counterpart on the pages; the
+ * pages do not discuss memory ownership of the kernels).
+ *
+ * Same computation and arguments as pa_decode, minus the workspace.  It is for
+ * callers that cannot allocate device memory themselves: a plugin or host
+ * framework that hands over only input and output buffers, or a latency-critical
+ * path where cudaMalloc / cudaFree (which may synchronise the device) are not
+ * allowed.  The scratch lives in one static 16 MiB device array inside libpa.so;
+ * every GPU that loads the library holds it until the process exits.  This call
+ * allocates nothing and calls no allocating routine.
+ *
+ *  - Limit: the batch must fit the 16 MiB scratch: 256 + 4 (num_seqs + 2)
+ *    (rounded up to 256) + 4160 (W + num_seqs * num_kv_heads * ceil(G / 8))
+ *    bytes, W = pa_default_workers() (1216 on a 152-SM GB300, which allows
+ *    about 2800 sequence x KV-head units, e.g. 350 sequences with 8 KV heads).
+ *    Larger batches return PA_ERR_WORKSPACE with the sizes in pa_last_error().
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current and caches it; make that
+ *    first call before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents;
+ *    each call clears the part that must start at zero (the status word) on its
+ *    stream.  Calls that may overlap on the GPU (other streams, other threads)
+ *    race on the array and give undefined results: serialise them.
+ *  - Device-side reports (PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT) stay in the
+ *    static array and are not returned by this call.
+ */
+PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                                   const float* k_scale, const float* v_scale, pa_stream_t stream);
+
+/*
  * Reads (and clears) the device-side status word of a workspace.  Synchronises
  * `stream`.  Returns PA_OK, PA_ERR_OUT_OF_RANGE or PA_ERR_TIMEOUT (the first
  * recorded, timeouts first), or PA_ERR_CUDA if the copy failed.

@@ -67,6 +67,8 @@ def _lib():
     lib.pa_decode_ex.restype = I
     lib.pa_mixed.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
     lib.pa_mixed.restype = I
+    lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P]
+    lib.pa_decode_noalloc.restype = I
     lib.pa_read_device_status.argtypes = [P, P]
     lib.pa_read_device_status.restype = I
     lib.pa_selftest_wait_timeout.argtypes = [P, Z, ctypes.c_uint, P]
@@ -181,6 +183,27 @@ def pa_mixed(out, q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, 
                          Hkv, d, bs, nb, float(scale), _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale),
                          _ptr(v_scale), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "pa_mixed")
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale=None, v_scale=None,
+                      stream=None):
+    """pa_decode for callers that cannot allocate: no workspace argument; the library's
+    static device scratch is used instead (see include/pa.h for its limit and rules)."""
+    _need(q, "q", (torch.bfloat16, torch.float16))
+    _need(out, "out", (q.dtype,))
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, tuple(_DTYPE))
+    _need(block_tables, "block_tables", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    B, Hq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    if out.shape != q.shape or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    st = _lib().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, d, bs, nb, float(scale),
+                                  _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale), _ptr(v_scale),
+                                  _stream(stream))
+    _check(st, "pa_decode_noalloc")
 
 
 def pa_read_device_status(workspace, stream=None) -> int:

@@ -282,6 +282,41 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_kv_heads, int head
     return l;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free decode: scratch in a fixed device array of this library.
+// ---------------------------------------------------------------------------
+
+// Scratch of pa_decode_noalloc.  Every GPU that loads the library holds these
+// 16 MiB until the process exits.  In host code the name below only stands in
+// for the device array; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[16u << 20];
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 16u << 20;
+std::map<int, void*> g_noalloc_address;   // device -> device address of g_noalloc_scratch
+
+// Device address of the static scratch on the current device, looked up once per
+// device (with that device current) and cached.
+pa_status noalloc_scratch(void** out, DeviceState** st_out) {
+    int dev = 0;
+    DeviceState* st = device_state(&dev);
+    if (!st) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_noalloc_address.find(dev);
+    if (it == g_noalloc_address.end()) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr) return fail("cudaGetSymbolAddress(scratch)", e);
+        it = g_noalloc_address.emplace(dev, ptr).first;
+    }
+    *out = it->second;
+    *st_out = st;
+    return PA_OK;
+}
+
+}  // namespace
+
 }  // namespace pa
 
 using namespace pa;
@@ -396,6 +431,38 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
     return decode_impl(out, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                        num_seqs, num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale,
                        workspace, workspace_bytes, 0, num_blocks, cs);
+}
+
+pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                            const float* k_scale, const float* v_scale, pa_stream_t stream) {
+    void* scratch = nullptr;
+    DeviceState* st = nullptr;
+    pa_status s = noalloc_scratch(&scratch, &st);
+    if (s != PA_OK) return s;
+    s = check_attention_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, q_dtype,
+                             cache_dtype, k_scale, v_scale, scratch);
+    if (s != PA_OK) return s;
+    if (num_seqs == 0) return PA_OK;
+    // the largest worker count this device can use bounds the scratch a call needs
+    const size_t need = decode_workspace_layout(num_seqs, num_kv_heads, head_groups_of(num_q_heads, num_kv_heads),
+                                                max_workers(*st)).total;
+    if (need > kNoAllocScratchBytes) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "pa_decode_noalloc: this batch needs %zu bytes of scratch; the static scratch holds %zu",
+                 need, kNoAllocScratchBytes);
+        return PA_ERR_WORKSPACE;
+    }
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // the device status word must start at zero; the rest is written before it is read
+    s = cuda_status(cudaMemsetAsync(scratch, 0, 256, cs), "cudaMemsetAsync(scratch status)");
+    if (s != PA_OK) return s;
+    return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                       num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, scratch,
+                       kNoAllocScratchBytes, 0, num_blocks, cs);
 }
 
 pa_status pa_read_device_status(void* workspace, pa_stream_t stream) {
