@@ -478,7 +478,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
 // where worker i left its unnormalised output o_i, running max m_i (log2 units)
 // and running sum l_i.  One CTA per unit, one warp per 16-wide slice of d.
 // Pass 1 reads every slot's (m, l) with lanes in parallel and reduces over the
-// warp; pass 2 reads up to 16 slots' fragments per round trip.
+// warp; pass 2 reads up to 16 slots' fragments per round trip, the first 16
+// requested together with pass 1.
 template <bool OutBf16, bool Fp8Layout>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
     grid_dependency_wait();
@@ -496,6 +497,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
     if (wa == wb) return;   // its only worker wrote the output
     const int nseg = wb - wa + 1;
     const int dt = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
+
+    // first batch of fragments and every slot's (m, l) are requested together
+    float4 v[16];
+    float m0v[16], m1v[16];
+    auto load_batch = [&](int base) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int sl = wa + min(base + k, nseg - 1) + u;
+            v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
+            m0v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t);
+            m1v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t + 1);
+        }
+    };
+    load_batch(0);
 
     float Mh[8], Lh[8];
 #pragma unroll
@@ -538,15 +553,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int base = 0; base < nseg; base += 16) {
-        float4 v[16];
-        float m0v[16], m1v[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int sl = wa + min(base + k, nseg - 1) + u;
-            v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
-            m0v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t);
-            m1v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t + 1);
-        }
+        if (base > 0) load_batch(base);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             if (base + k < nseg) {
