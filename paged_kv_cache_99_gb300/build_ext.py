@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["pa_api.cu", "decode.cu", "mixed.cu", "reshape_and_cache.cu", "selftest.cu"]
+SOURCES = ["pa_api.cu", "decode.cu", "chunk_tc.cu", "reshape_and_cache.cu", "selftest.cu"]
 HEADERS = ["pa_device.cuh", "pa_internal.h"]
 BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB_PATH = os.path.join(BUILD_DIR, "libpa.so")

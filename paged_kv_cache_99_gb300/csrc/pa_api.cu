@@ -222,8 +222,9 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     return cuda_status(launch_combine(q_bf16, kind == kKindFp8, p, stream), "launch(combine)");
 }
 
-pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, const CUtensorMap& kmap,
-                     const CUtensorMap& vmap, const int32_t* block_tables, int max_blocks_per_seq,
+pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
+                     const void* v_cache, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* seq_lens, int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
                      int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
                      const float* v_scale, void* workspace, cudaStream_t stream) {
@@ -250,6 +251,8 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.out = out;
     p.q = q;
     p.query_start_loc = query_start_loc;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.k_scale = k_scale;
@@ -423,7 +426,7 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
         if (s != PA_OK) return s;
         s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, kind == kKindFp8);
         if (s != PA_OK) return s;
-        s = chunk_impl(out, q, query_start_loc, kmap, vmap, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+        s = chunk_impl(out, q, query_start_loc, k_cache, v_cache, kmap, vmap, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        total_q, num_q_heads, num_kv_heads, num_blocks, scale, q_dtype, cache_dtype, k_scale,
                        v_scale, workspace, cs);
         if (s != PA_OK) return s;

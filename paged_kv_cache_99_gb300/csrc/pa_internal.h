@@ -54,6 +54,8 @@ struct DecodeParams {
 struct ChunkParams {
     void* out;
     const void* q;
+    const void* k_cache;              // read directly by the FP8 path
+    const void* v_cache;
     const int32_t* query_start_loc;
     const int32_t* block_tables;
     const int32_t* seq_lens;
