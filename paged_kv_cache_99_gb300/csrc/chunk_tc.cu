@@ -5,23 +5,24 @@
 // conversations"): row j of a chunk of q_len new tokens sits at position
 // seq_len - q_len + j and attends causally to tokens 0..pos of its own sequence,
 // reached through the block table.  For a prompt chunk this is a dense
-// contraction: 128 query rows against every cached key.
+// contraction of the query rows against every cached key.
 //
-// One CTA = 128 MMA rows (consecutive queries x all heads of one KV head, so
-// each K/V tile in shared memory serves the whole GQA group) of one chunk; keys
-// advance 128 at a time (8 blocks).
-//   warp 0      producer: bulk tensor copies (TMA, 128-byte swizzle) of the
-//               step's K and V blocks, 16-bit caches
-//   warp 1      one lane issues tcgen05.mma: S_i = Q K_i^T into one of two
-//               tensor-memory buffers, then O += P_{i-1} V_{i-1} (pipelined so
-//               that S_i runs while softmax works on step i-1)
-//   warps 2-5   softmax, one thread per row (no shuffles): S from tensor
-//               memory, causal mask, online max/sum, P to shared memory; O is
-//               rescaled in tensor memory only when a row maximum grows by more
-//               than 2^8 (otherwise the old maximum keeps serving)
-//   warps 6-9   FP8 caches only: gather e4m3 rows through the block table,
-//               widen them exactly to f16 and store them in the MMA layout
-// Accumulators (S x2, O) live in tensor memory; every wait is bounded.
+// One CTA = two consecutive tiles A and B of 128 MMA rows each (queries x all
+// heads of one KV head, so every K/V tile in shared memory serves the whole
+// GQA group twice) of one chunk; keys advance 64 at a time (4 blocks) through a
+// 3-stage ring.  While one softmax warpgroup works on its tile, the tensor core
+// runs the other tile's products (ping-pong).
+//   warp 0       producer: bulk tensor copies (TMA, 128-byte swizzle) of each
+//                step's K and V blocks (16-bit caches), one lane per block
+//   warp 1       one lane issues tcgen05.mma: S_X(i) = Q_X K_i^T into a double
+//                buffer in tensor memory, then O_X += P_X(i-1) V_(i-1)
+//   warps 2-5    softmax of tile A, warps 6-9 softmax of tile B: one thread
+//                per row, S from tensor memory, causal mask, online max/sum,
+//                P to shared memory; O rescaled in tensor memory only when a
+//                row maximum grows by more than 2^8
+//   warps 10-13  FP8 caches only: gather e4m3 rows through the block table, widen
+//                them exactly to f16 and store them in the MMA layout
+// Every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -32,29 +33,40 @@ namespace pa {
 
 namespace {
 
-constexpr int kTcRows = 128;                 // MMA M
-constexpr int kTcKeys = 128;                 // keys per step (MMA N of S, K of PV)
+constexpr int kTcRows = 128;                 // MMA M of one tile
+constexpr int kTcKeys = 64;                  // keys per step (MMA N of S, K of PV)
 constexpr int kTcBlocksPerStep = kTcKeys / kBlockSize;
-constexpr uint32_t kHalfBytes = 16384;       // [128 rows][64 elements] of one d-half
-constexpr uint32_t kOffQ = 0;                // Q: two d-halves
-constexpr uint32_t kOffStage = 32768;        // stage s: K at +65536 s, V 32 KiB after it
-constexpr uint32_t kStageBytes = 65536;
-constexpr uint32_t kOffP = kOffStage + 2 * kStageBytes;   // P: two key-halves
-constexpr uint32_t kOffBars = kOffP + 32768;
-constexpr uint32_t kBarBytes = 128;          // 11 barriers + tensor-memory address
+constexpr int kTcStages = 3;
+constexpr uint32_t kQHalf = 16384;           // Q tile: [128 rows][64 elements] per d-half
+constexpr uint32_t kKvHalf = 8192;           // K or V of a step: [64 rows][64 elements] per d-half
+constexpr uint32_t kOffQ = 0;                // Q_A, Q_B: 32 KiB each
+constexpr uint32_t kOffStage = 65536;        // stage s: K at +32768 s, V 16 KiB after it
+constexpr uint32_t kStageBytes = 32768;
+constexpr uint32_t kOffP = kOffStage + kTcStages * kStageBytes;   // P_A, P_B: [128 rows][64 keys]
+constexpr uint32_t kPBytes = 16384;
+constexpr uint32_t kOffBars = kOffP + 2 * kPBytes;
+constexpr uint32_t kBarBytes = 256;          // barriers + tensor-memory address
 constexpr uint32_t kOffCum = kOffBars + kBarBytes;
-constexpr uint32_t kTmemCols = 512;          // S0 at 0, S1 at 128, O at 256
+constexpr uint32_t kTmemCols = 512;          // S_A 0,64  S_B 128,192  O_A 256  O_B 384
 constexpr float kRescaleLog2 = 8.0f;         // lazy rescale threshold (factor 256)
 
 // barrier indices (8 bytes each from kOffBars)
-enum { kBarKvFull = 0, kBarKvEmpty = 2, kBarSFull = 4, kBarSFree = 6, kBarPFull = 8, kBarPvDone = 9,
-       kBarQFull = 10 };
+enum {
+    kBarKvFull = 0,     // [3]
+    kBarKvEmpty = 3,    // [3]
+    kBarSFull = 6,      // [tile][2]
+    kBarSFree = 10,     // [tile][2]
+    kBarPFull = 14,     // [tile]
+    kBarPvDone = 16,    // [tile]
+    kBarQFull = 18,
+    kNumBars = 19
+};
 
 template <int Kind>
 struct TcCfg {
     static constexpr bool kFp8 = Kind == kKindFp8;
     static constexpr bool kMmaBf16 = Kind == kKindBf16;
-    static constexpr int kWarps = kFp8 ? 10 : 6;
+    static constexpr int kWarps = kFp8 ? 14 : 10;
 };
 
 // Bounded wait by lane 0 of the warp, then an acquire by every lane.
@@ -67,6 +79,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
 }
 
 }  // namespace
+
 
 template <int Kind, bool QBf16>
 __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
@@ -83,21 +96,25 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (sbase - raw_base);
     int* cum = reinterpret_cast<int*>(sm + kOffCum);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBars + 11 * 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBars + kNumBars * 8);
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8u * i; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kTcStages; ++s) {
             mbar_init(bar(kBarKvFull + s), kFp8 ? 4 : 1);
             mbar_init(bar(kBarKvEmpty + s), 1);
-            mbar_init(bar(kBarSFull + s), 1);
-            mbar_init(bar(kBarSFree + s), 4);
         }
-        mbar_init(bar(kBarPFull), 4);
-        mbar_init(bar(kBarPvDone), 1);
-        mbar_init(bar(kBarQFull), 4);
+        for (int x = 0; x < 2; ++x) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(bar(kBarSFull + 2 * x + b), 1);
+                mbar_init(bar(kBarSFree + 2 * x + b), 4);
+            }
+            mbar_init(bar(kBarPFull + x), 4);
+            mbar_init(bar(kBarPvDone + x), 1);
+        }
+        mbar_init(bar(kBarQFull), 8);
         fence_barrier_init();
         if constexpr (!kFp8) {
             tmap_prefetch(&kmap);
@@ -107,19 +124,19 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
 
     grid_dependency_wait();
 
-    // ---- tiles per chunk sequence, exclusive scan -> cum ----
+    // ---- tile pairs per chunk sequence, exclusive scan -> cum ----
     const int B = p.num_seqs;
     const int QT = p.queries_per_tile;
-    auto tiles_of = [&](int s) -> int {
+    auto pairs_of = [&](int s) -> int {
         const int ql = p.query_start_loc[s + 1] - p.query_start_loc[s];
-        return ql >= 2 ? (ql + QT - 1) / QT : 0;
+        return ql >= 2 ? (ql + 2 * QT - 1) / (2 * QT) : 0;
     };
     {
         const int per = (B + kThreads - 1) / kThreads;
         const int beg = min(B, static_cast<int>(threadIdx.x) * per);
         const int end = min(B, beg + per);
         int local = 0;
-        for (int s = beg; s < end; ++s) local += tiles_of(s);
+        for (int s = beg; s < end; ++s) local += pairs_of(s);
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -132,7 +149,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         for (int w = 0; w < warp; ++w) run += warp_tot[w];
         for (int s = beg; s < end; ++s) {
             cum[s] = run;
-            run += tiles_of(s);
+            run += pairs_of(s);
         }
         if (threadIdx.x == kThreads - 1) cum[B] = run;
     }
@@ -141,7 +158,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
 
     const int R = cum[B];
     if (static_cast<int>(blockIdx.x) >= R) return;
-    const int tau = R - 1 - static_cast<int>(blockIdx.x);   // heaviest tiles first
+    const int tau = R - 1 - static_cast<int>(blockIdx.x);   // heaviest pairs first
     int s = 0;
     {
         int lo = 0, hi = B;
@@ -151,23 +168,28 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         }
         s = lo;
     }
-    const int qt = tau - cum[s];
+    const int pair = tau - cum[s];
     const int h = blockIdx.y;
     const int G = p.group;
     const int q0 = p.query_start_loc[s];
     const int q_len = p.query_start_loc[s + 1] - q0;
     const int n = p.seq_lens[s];
-    const int j_first = qt * QT;
-    const int j_last = min(q_len, j_first + QT) - 1;
-    const int pos_first = n - q_len + j_first;
-    const int pos_last = n - q_len + j_last;
-    if (pos_first < 0 || n > p.max_blocks * kBlockSize) {   // inconsistent lengths
+    if (n - q_len < 0 || n > p.max_blocks * kBlockSize) {   // inconsistent lengths
         if (threadIdx.x == 0) atomicOr(p.status, kDevErrRange);
         return;
     }
-    const int nsteps = pos_last / kTcKeys + 1;
-    const int nblocks = pos_last / kBlockSize + 1;
+    // tile X (0 = A, 1 = B): queries j_first[X] .. j_last[X]; B may be absent
+    const int jf0 = 2 * pair * QT;
+    const int jf1 = jf0 + QT;
+    const bool has_b = jf1 < q_len;
+    const int jl0 = min(q_len, jf0 + QT) - 1;
+    const int jl1 = has_b ? min(q_len, jf1 + QT) - 1 : jl0;
+    const int pos_last_cta = n - q_len + jl1;
+    const int nsteps = pos_last_cta / kTcKeys + 1;
+    const int nsteps_a = (n - q_len + jl0) / kTcKeys + 1;
+    const int nblocks = pos_last_cta / kBlockSize + 1;
     const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+    auto tile_steps = [&](int x) -> int { return x == 0 ? nsteps_a : (has_b ? nsteps : 0); };
 
     // ---- tensor memory ----
     if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -175,14 +197,13 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS0 = tmem, tO = tmem + 256;
+    auto tS = [&](int x, int b) -> uint32_t { return tmem + 128u * x + 64u * b; };
+    auto tO = [&](int x) -> uint32_t { return tmem + 256u + 128u * x; };
     bool ok = true;
 
     if (warp == 0) {
-        // ================= producer (16-bit caches) =================
+        // ================= producer (16-bit caches): lane b < 4 copies block b of a step =================
         if constexpr (!kFp8) {
-            // lane b < 8 handles block b of each step: its table entry (loaded one
-            // step ahead) and its four tile copies
             auto entry = [&](int i) -> int {
                 const int j = i * kTcBlocksPerStep + lane;
                 int phys = 0;
@@ -197,25 +218,26 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             };
             int phys = entry(0);
             for (int i = 0; i < nsteps && ok; ++i) {
-                const int st = i & 1;
+                const int st = i % kTcStages;
                 const int phys_next = i + 1 < nsteps ? entry(i + 1) : 0;
-                if (i >= 2 && !warp_wait(bar(kBarKvEmpty + st), ((i >> 1) - 1) & 1, p.timeout_ns)) {
+                if (i >= kTcStages &&
+                    !warp_wait(bar(kBarKvEmpty + st), ((i / kTcStages) - 1) & 1, p.timeout_ns)) {
                     if (lane == 0) atomicOr(p.status, kDevErrTimeout);
                     ok = false;
                     break;
                 }
                 const int nb = min(kTcBlocksPerStep, nblocks - i * kTcBlocksPerStep);
                 const uint32_t kdst = sbase + kOffStage + st * kStageBytes;
-                const uint32_t vdst = kdst + 2 * kHalfBytes;
+                const uint32_t vdst = kdst + 2 * kKvHalf;
                 if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + st), static_cast<uint32_t>(nb) * 2 * 4096);
                 __syncwarp();
                 if (lane < nb) {
                     const int y = (phys * p.num_kv_heads + h) * kBlockSize;
                     // block b -> rows 16b..16b+15 of each d-half
                     tma_load_2d(kdst + lane * 2048, &kmap, 0, y, bar(kBarKvFull + st));
-                    tma_load_2d(kdst + kHalfBytes + lane * 2048, &kmap, 64, y, bar(kBarKvFull + st));
+                    tma_load_2d(kdst + kKvHalf + lane * 2048, &kmap, 64, y, bar(kBarKvFull + st));
                     tma_load_2d(vdst + lane * 2048, &vmap, 0, y, bar(kBarKvFull + st));
-                    tma_load_2d(vdst + kHalfBytes + lane * 2048, &vmap, 64, y, bar(kBarKvFull + st));
+                    tma_load_2d(vdst + kKvHalf + lane * 2048, &vmap, 64, y, bar(kBarKvFull + st));
                 }
                 phys = phys_next;
             }
@@ -225,60 +247,82 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_f16<kMmaBf16>(kTcRows, kTcKeys, false);
             constexpr uint32_t idPV = umma_idesc_f16<kMmaBf16>(kTcRows, kHeadDim, true);
-            auto pv = [&](int j) -> bool {
-                if (!mbar_wait_bounded(bar(kBarPFull), j & 1, p.timeout_ns)) return false;
+            auto issue_s = [&](int x, int i) -> bool {
+                const int sb = i & 1;
+                if (i >= 2 && !mbar_wait_bounded(bar(kBarSFree + 2 * x + sb), ((i >> 1) - 1) & 1, p.timeout_ns))
+                    return false;
                 tc_fence_after();
-                const uint32_t vbase = sbase + kOffStage + (j & 1) * kStageBytes + 2 * kHalfBytes;
+                const uint32_t qbase = sbase + kOffQ + x * 2 * kQHalf;
+                const uint32_t kbase = sbase + kOffStage + (i % kTcStages) * kStageBytes;
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    const uint64_t a = umma_desc_sw128(sbase + kOffP + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kHalfBytes, 1024);
-                    umma_f16(tO, a, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint64_t a = umma_desc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = umma_desc_sw128(kbase + (kk >> 2) * kKvHalf + (kk & 3) * 32, 16, 1024);
+                    umma_f16(tS(x, sb), a, b, idS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(kBarPvDone));
-                umma_commit(bar(kBarKvEmpty + (j & 1)));
+                umma_commit(bar(kBarSFull + 2 * x + sb));
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                // the last step of a 16-bit cache waits for every tile first: the softmax of the
+                // last tile zeroes V rows past the last position before signalling
+                const bool wait_all = !kFp8 && j == nsteps - 1;
+                if (wait_all) {
+                    for (int x = 0; x < 2; ++x)
+                        if (j < tile_steps(x) && !mbar_wait_bounded(bar(kBarPFull + x), j & 1, p.timeout_ns))
+                            return false;
+                }
+                const uint32_t vbase = sbase + kOffStage + (j % kTcStages) * kStageBytes + 2 * kKvHalf;
+                for (int x = 0; x < 2; ++x) {
+                    if (j >= tile_steps(x)) continue;
+                    if (!wait_all && !mbar_wait_bounded(bar(kBarPFull + x), j & 1, p.timeout_ns)) return false;
+                    tc_fence_after();
+                    const uint32_t pbase = sbase + kOffP + x * kPBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                        const uint64_t a = umma_desc_sw128(pbase + kk * 32, 16, 1024);
+                        const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
+                        umma_f16(tO(x), a, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar(kBarPvDone + x));
+                }
+                umma_commit(bar(kBarKvEmpty + (j % kTcStages)));
                 return true;
             };
             ok = mbar_wait_bounded(bar(kBarQFull), 0, p.timeout_ns);
             for (int i = 0; i < nsteps && ok; ++i) {
-                const int st = i & 1;
-                if (!mbar_wait_bounded(bar(kBarKvFull + st), (i >> 1) & 1, p.timeout_ns) ||
-                    (i >= 2 && !mbar_wait_bounded(bar(kBarSFree + st), ((i >> 1) - 1) & 1, p.timeout_ns))) {
+                if (!mbar_wait_bounded(bar(kBarKvFull + i % kTcStages), (i / kTcStages) & 1, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t kbase = sbase + kOffStage + st * kStageBytes;
-#pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    const uint64_t a = umma_desc_sw128(sbase + kOffQ + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = umma_desc_sw128(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    umma_f16(tS0 + st * kTcKeys, a, b, idS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(bar(kBarSFull + st));
-                if (i >= 1 && !pv(i - 1)) {
-                    ok = false;
-                    break;
-                }
+                for (int x = 0; x < 2 && ok; ++x)
+                    if (i < tile_steps(x)) ok = issue_s(x, i);
+                if (ok && i >= 1) ok = issue_pv(i - 1);
             }
-            if (ok && !pv(nsteps - 1)) ok = false;
+            if (ok) ok = issue_pv(nsteps - 1);
             if (!ok) atomicOr(p.status, kDevErrTimeout);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ================= softmax: thread = one MMA row =================
+    } else if (warp < 10) {
+        // ================= softmax: warps 2-5 tile A, 6-9 tile B; thread = one MMA row =================
+        const int x = warp < 6 ? 0 : 1;
         const int quarter = warp & 3;                  // tensor-memory lanes 32 quarter .. + 31
         const int r = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const int steps = tile_steps(x);
+        const int jf = x == 0 ? jf0 : jf1;
+        const int jl = x == 0 ? jl0 : jl1;
         const int jq = r / G;
-        const bool live = r < QT * G && j_first + jq <= j_last;
-        const int pos = live ? n - q_len + j_first + jq : pos_last;
-        const size_t qrow = (static_cast<size_t>(q0 + (live ? j_first + jq : j_first)) * p.num_q_heads + h * G +
+        const bool live = steps > 0 && r < QT * G && jf + jq <= jl;
+        const int pos_first = n - q_len + jf;
+        const int pos = live ? n - q_len + jf + jq : n - q_len + jl;
+        const size_t qrow = (static_cast<size_t>(q0 + (live ? jf + jq : jf0)) * p.num_q_heads + h * G +
                              (live ? r % G : 0)) * kHeadDim;
         // Q row -> shared memory (MMA input type), 128-byte swizzle, two d-halves
         {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qrow);
-#pragma unroll
+            uint8_t* qdst = sm + kOffQ + x * 2 * kQHalf;
+#pragma unroll 4
             for (int c = 0; c < 16; ++c) {
                 uint4 v = live ? src[c] : make_uint4(0, 0, 0, 0);
                 if constexpr (kFp8 && QBf16) {
@@ -288,7 +332,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                         w[e] = pack2<false>(to_float<true>(w[e] & 0xffffu), to_float<true>(w[e] >> 16));
                     v = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                *reinterpret_cast<uint4*>(sm + kOffQ + (c >> 3) * kHalfBytes + sw128_offset(r, (c & 7) * 8)) = v;
+                *reinterpret_cast<uint4*>(qdst + (c >> 3) * kQHalf + sw128_offset(r, (c & 7) * 8)) = v;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -297,22 +341,22 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         const float kscale = kFp8 ? __ldg(p.k_scale) : 1.0f;
         const float vscale = kFp8 ? __ldg(p.v_scale) : 1.0f;
         const float s_log2 = p.scale_log2 * kscale;
+        const bool pos_scale = s_log2 >= 0.f;
         float m_used = -INFINITY, l = 0.f;
-        for (int i = 0; i < nsteps && ok; ++i) {
-            const int st = i & 1;
-            if (!warp_wait(bar(kBarSFull + st), (i >> 1) & 1, p.timeout_ns)) {
+        for (int i = 0; i < steps && ok; ++i) {
+            const int sb = i & 1;
+            if (!warp_wait(bar(kBarSFull + 2 * x + sb), (i >> 1) & 1, p.timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int key0 = i * kTcKeys;
             const bool need_mask = key0 + kTcKeys - 1 > pos_first;
-            const uint32_t s_addr = tS0 + st * kTcKeys + lane_off;
-            // pass 1: row maximum of the raw scores (scaled once: scale > 0 keeps the
-            // order, scale < 0 reverses it), 32 columns at a time
-            const bool pos_scale = s_log2 >= 0.f;
             const int lim = pos - key0;                 // columns > lim are masked
+            const uint32_t s_addr = tS(x, sb) + lane_off;
+            // pass 1: row maximum of the raw scores (scale > 0 keeps the order, < 0 reverses it)
             float hi = -INFINITY, lo = INFINITY;
+#pragma unroll
             for (int c = 0; c < kTcKeys / 32; ++c) {
                 uint32_t sv[32];
                 tmem_ld32(s_addr + 32 * c, sv);
@@ -336,24 +380,24 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             const bool need = mx > m_used + kRescaleLog2;
             const bool resc = __any_sync(0xffffffffu, need);
             const float m_new = need ? fmaxf(m_used, mx) : m_used;
-            const float alpha = ex2_approx(m_used - m_new);   // 0 on the first step, 1 when kept
+            const float alpha = ex2_approx(m_used - m_new);    // 0 on the first step, 1 when kept
             m_used = m_new;
-            // P buffer and O are busy until the previous step's P.V is done
+            // P buffer and O are busy until this tile's previous P.V is done
             if (i >= 1) {
-                if (!warp_wait(bar(kBarPvDone), (i - 1) & 1, p.timeout_ns)) {
+                if (!warp_wait(bar(kBarPvDone + x), (i - 1) & 1, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (resc) {
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < kHeadDim / 32; ++c) {
                         uint32_t ov[32];
-                        tmem_ld32(tO + lane_off + 32 * c, ov);
+                        tmem_ld32(tO(x) + lane_off + 32 * c, ov);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(tO + lane_off + 32 * c, ov);
+                        tmem_st32(tO(x) + lane_off + 32 * c, ov);
                     }
                     tmem_wait_st();
                 }
@@ -361,6 +405,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             // pass 2: p = 2^(s * scale - m), stored as the A operand of P.V
             float sum = 0.f;
             const float neg_m = -m_new;
+            uint8_t* prow = sm + kOffP + x * kPBytes;
+#pragma unroll
             for (int c = 0; c < kTcKeys / 32; ++c) {
                 uint32_t sv[32];
                 tmem_ld32(s_addr + 32 * c, sv);
@@ -380,29 +426,29 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                         sum += p0 + p1;
                         w[k] = pack2<kMmaBf16>(p0, p1);
                     }
-                    const int chunk = 4 * c + q4;   // keys 8 chunk .. + 7
-                    *reinterpret_cast<uint4*>(sm + kOffP + (chunk >> 3) * kHalfBytes + sw128_offset(r, (chunk & 7) * 8)) =
+                    *reinterpret_cast<uint4*>(prow + sw128_offset(r, (4 * c + q4) * 8)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSFree + st));
+            if (lane == 0) mbar_arrive(bar(kBarSFree + 2 * x + sb));
             l = l * alpha + sum;
             if constexpr (!kFp8) {
-                // keys past the tile's last position get P = 0, but their V rows hold
-                // unloaded (stale) or poisoned bytes and 0 x NaN is NaN: zero them
-                if (key0 + kTcKeys - 1 > pos_last) {
-                    if (!warp_wait(bar(kBarKvFull + st), (i >> 1) & 1, p.timeout_ns)) {
+                // keys past the CTA's last position get P = 0, but their V rows hold unloaded
+                // (stale) or poisoned bytes and 0 x NaN is NaN: the last tile zeroes them
+                if (i == nsteps - 1 && x == (has_b ? 1 : 0)) {
+                    const int st = i % kTcStages;
+                    if (!warp_wait(bar(kBarKvFull + st), (i / kTcStages) & 1, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    if (key0 + r > pos_last) {
-                        uint8_t* vrow = sm + kOffStage + st * kStageBytes + 2 * kHalfBytes + r * 128;
+                    if (r < kTcKeys && key0 + r > pos_last_cta) {
+                        uint8_t* vrow = sm + kOffStage + st * kStageBytes + 2 * kKvHalf + r * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
-                            *reinterpret_cast<uint4*>(vrow + kHalfBytes + 16 * c) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(vrow + kKvHalf + 16 * c) = make_uint4(0, 0, 0, 0);
                         }
                     }
                 }
@@ -410,94 +456,99 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarPFull));
+            if (lane == 0) mbar_arrive(bar(kBarPFull + x));
         }
         // ---- epilogue: O / l ----
-        if (ok && warp_wait(bar(kBarPvDone), (nsteps - 1) & 1, p.timeout_ns)) {
-            tc_fence_after();
-            const float inv = vscale / l;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow);
+        if (steps > 0) {
+            if (ok && warp_wait(bar(kBarPvDone + x), (steps - 1) & 1, p.timeout_ns)) {
+                tc_fence_after();
+                const float inv = vscale / l;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow);
+#pragma unroll 1
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO(x) + lane_off + 32 * c, ov);
+                    tmem_wait_ld();
+                    if (live) {
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 32; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(tO + lane_off + 32 * c, ov);
-                tmem_wait_ld();
-                if (live) {
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            w[k] = static_cast<uint32_t>(from_float<QBf16>(__uint_as_float(ov[8 * e + 2 * k]) * inv)) |
-                                   (static_cast<uint32_t>(from_float<QBf16>(__uint_as_float(ov[8 * e + 2 * k + 1]) * inv)) << 16);
-                        dst[4 * c + e] = make_uint4(w[0], w[1], w[2], w[3]);
+                            for (int k = 0; k < 4; ++k)
+                                w[k] = static_cast<uint32_t>(from_float<QBf16>(__uint_as_float(ov[8 * e + 2 * k]) * inv)) |
+                                       (static_cast<uint32_t>(from_float<QBf16>(__uint_as_float(ov[8 * e + 2 * k + 1]) * inv)) << 16);
+                            dst[4 * c + e] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
                 }
+            } else if (lane == 0) {
+                atomicOr(p.status, kDevErrTimeout);
             }
-        } else if (lane == 0) {
-            atomicOr(p.status, kDevErrTimeout);
         }
     } else if constexpr (kFp8) {
-        // ================= FP8 converters: thread = one key row of the step =================
-        const int c = threadIdx.x - 6 * 32;            // 0..127
+        // ================= FP8 converters: thread = half a key row (64 d) of the step =================
+        const int c = threadIdx.x - 10 * 32;           // 0..127
+        const int krow = c >> 1;                       // key within the step
+        const int half = c & 1;                        // d-half
         const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
         const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
-        auto load_row = [&](int i, uint4 (&kx)[8], uint4 (&vx)[8]) {
-            const int key = i * kTcKeys + c;
-            if (key <= pos_last) {          // later keys get P = 0: store zeros
+        auto load_row = [&](int i, uint4 (&kx)[4], uint4 (&vx)[4]) {
+            const int key = i * kTcKeys + krow;
+            if (key <= pos_last_cta) {      // later keys get P = 0: store zeros
                 int phys = __ldg(bt + (key >> 4));
                 if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
                     atomicOr(p.status, kDevErrRange);
                     phys = 0;
                 }
-                const size_t off = ((static_cast<size_t>(phys) * p.num_kv_heads + h) * kBlockSize + (key & 15)) * kHeadDim;
+                const size_t off =
+                    ((static_cast<size_t>(phys) * p.num_kv_heads + h) * kBlockSize + (key & 15)) * kHeadDim + 64 * half;
                 const uint4* ks = reinterpret_cast<const uint4*>(kc + off);
                 const uint4* vs = reinterpret_cast<const uint4*>(vc + off);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 4; ++e) {
                     kx[e] = __ldg(ks + e);
                     vx[e] = __ldg(vs + e);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) kx[e] = vx[e] = make_uint4(0, 0, 0, 0);
+                for (int e = 0; e < 4; ++e) kx[e] = vx[e] = make_uint4(0, 0, 0, 0);
             }
         };
-        auto widen_store = [&](uint8_t* dst, const uint4 (&x)[8]) {
-            // 16 e4m3 codes (d = 16e .. 16e + 15) -> 16 exact f16 values, 128-byte swizzle
+        auto widen_store = [&](uint8_t* dst, const uint4 (&x4)[4]) {
+            // 64 e4m3 codes (d = 64 half + 16e ..) -> exact f16, 128-byte swizzle
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t w[4] = {x[e].x, x[e].y, x[e].z, x[e].w};
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t w[4] = {x4[e].x, x4[e].y, x4[e].z, x4[e].w};
                 uint32_t f[8];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     f[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
                     f[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
                 }
-                const int d0 = 16 * e;   // chunks d0/8 and d0/8 + 1
-                *reinterpret_cast<uint4*>(dst + (d0 >> 6) * kHalfBytes + sw128_offset(c, d0 & 63)) =
+                *reinterpret_cast<uint4*>(dst + half * kKvHalf + sw128_offset(krow, 16 * e)) =
                     make_uint4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<uint4*>(dst + (d0 >> 6) * kHalfBytes + sw128_offset(c, (d0 & 63) + 8)) =
+                *reinterpret_cast<uint4*>(dst + half * kKvHalf + sw128_offset(krow, 16 * e + 8)) =
                     make_uint4(f[4], f[5], f[6], f[7]);
             }
         };
-        uint4 kx[8], vx[8], kn[8], vn[8];
+        uint4 kx[4], vx[4], kn[4], vn[4];
         load_row(0, kx, vx);
         for (int i = 0; i < nsteps && ok; ++i) {
-            const int st = i & 1;
+            const int st = i % kTcStages;
             if (i + 1 < nsteps) load_row(i + 1, kn, vn);          // in flight while this step converts
-            if (i >= 2 && !warp_wait(bar(kBarKvEmpty + st), ((i >> 1) - 1) & 1, p.timeout_ns)) {
+            if (i >= kTcStages &&
+                !warp_wait(bar(kBarKvEmpty + st), ((i / kTcStages) - 1) & 1, p.timeout_ns)) {
                 ok = false;
                 break;
             }
             uint8_t* kdst = sm + kOffStage + st * kStageBytes;
             widen_store(kdst, kx);
-            widen_store(kdst + 2 * kHalfBytes, vx);
+            widen_store(kdst + 2 * kKvHalf, vx);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarKvFull + st));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < 4; ++e) {
                 kx[e] = kn[e];
                 vx[e] = vn[e];
             }
@@ -536,6 +587,8 @@ size_t chunk_smem_bytes(CacheKind, int num_seqs) {
 }
 
 int chunk_rows() { return kTcRows; }
+
+int chunk_tiles_per_cta() { return 2; }
 
 cudaError_t chunk_prepare(CacheKind kind, bool q_bf16, size_t max_smem) {
     cudaFuncAttributes fa;

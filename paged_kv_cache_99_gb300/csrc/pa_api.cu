@@ -245,7 +245,8 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
             st->chunk_prepared[kind][q_bf16] = true;
         }
     }
-    const long long grid_x = static_cast<long long>(num_seqs) + (total_q + qt - 1) / qt;
+    const int per_cta = qt * chunk_tiles_per_cta();   // queries of one chunk per CTA
+    const long long grid_x = static_cast<long long>(num_seqs) + (total_q + per_cta - 1) / per_cta;
     if (grid_x >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     ChunkParams p;
     p.out = out;

@@ -100,7 +100,8 @@ cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_
 
 // Prefill chunks.
 size_t chunk_smem_bytes(CacheKind kind, int num_seqs);
-int chunk_rows();
+int chunk_rows();           // MMA rows of one query tile
+int chunk_tiles_per_cta();  // query tiles one CTA processes
 cudaError_t chunk_prepare(CacheKind kind, bool q_bf16, size_t max_smem);
 cudaError_t launch_chunk(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, const ChunkParams& p, int grid_x, size_t smem,
