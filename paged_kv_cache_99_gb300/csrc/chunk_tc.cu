@@ -263,43 +263,61 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 umma_commit(bar(kBarSFull + 2 * x + sb));
                 return true;
             };
-            auto issue_pv = [&](int j) -> bool {
-                // the last step of a 16-bit cache waits for every tile first: the softmax of the
-                // last tile zeroes V rows past the last position before signalling
-                const bool wait_all = !kFp8 && j == nsteps - 1;
-                if (wait_all) {
-                    for (int x = 0; x < 2; ++x)
-                        if (j < tile_steps(x) && !mbar_wait_bounded(bar(kBarPFull + x), j & 1, p.timeout_ns))
-                            return false;
-                }
+            auto issue_pv = [&](int x, int j) {
                 const uint32_t vbase = sbase + kOffStage + (j % kTcStages) * kStageBytes + 2 * kKvHalf;
-                for (int x = 0; x < 2; ++x) {
-                    if (j >= tile_steps(x)) continue;
-                    if (!wait_all && !mbar_wait_bounded(bar(kBarPFull + x), j & 1, p.timeout_ns)) return false;
-                    tc_fence_after();
-                    const uint32_t pbase = sbase + kOffP + x * kPBytes;
+                const uint32_t pbase = sbase + kOffP + x * kPBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                        const uint64_t a = umma_desc_sw128(pbase + kk * 32, 16, 1024);
-                        const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
-                        umma_f16(tO(x), a, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(bar(kBarPvDone + x));
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    const uint64_t a = umma_desc_sw128(pbase + kk * 32, 16, 1024);
+                    const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
+                    umma_f16(tO(x), a, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(kBarKvEmpty + (j % kTcStages)));
-                return true;
+                umma_commit(bar(kBarPvDone + x));
             };
+            // Event loop: poll the barriers and issue whatever is ready, P.V first (it
+            // unblocks that tile's softmax), then the next S into a free buffer, so that
+            // one tile never waits behind the other.  No barrier can move past the
+            // phase tested here: each one's next phase needs an MMA not yet issued.
+            const int zt = has_b ? 1 : 0;             // tile that zeroes V rows in the last step
+            int next_s[2] = {0, 0}, next_pv[2] = {0, 0};
             ok = mbar_wait_bounded(bar(kBarQFull), 0, p.timeout_ns);
-            for (int i = 0; i < nsteps && ok; ++i) {
-                if (!mbar_wait_bounded(bar(kBarKvFull + i % kTcStages), (i / kTcStages) & 1, p.timeout_ns)) {
-                    ok = false;
-                    break;
+            uint64_t t_last = global_timer_ns();
+            while (ok && (next_pv[0] < tile_steps(0) || next_pv[1] < tile_steps(1))) {
+                bool progress = false;
+                for (int x = 0; x < 2; ++x) {
+                    const int j = next_pv[x];
+                    if (j < tile_steps(x) && j < next_s[x] && mbar_test(bar(kBarPFull + x), j & 1)) {
+                        // a 16-bit cache's last step also waits for the zeroing tile
+                        const bool blocked = !kFp8 && j == nsteps - 1 && x != zt && j < tile_steps(zt) &&
+                                             !(next_pv[zt] > j || mbar_test(bar(kBarPFull + zt), j & 1));
+                        if (!blocked) {
+                            tc_fence_after();
+                            issue_pv(x, j);
+                            next_pv[x] = j + 1;
+                            progress = true;
+                            const int other = 1 - x;
+                            if (j >= tile_steps(other) || next_pv[other] > j)
+                                umma_commit(bar(kBarKvEmpty + (j % kTcStages)));   // both tiles done with stage
+                        }
+                    }
                 }
-                for (int x = 0; x < 2 && ok; ++x)
-                    if (i < tile_steps(x)) ok = issue_s(x, i);
-                if (ok && i >= 1) ok = issue_pv(i - 1);
+                for (int x = 0; x < 2; ++x) {
+                    const int i = next_s[x];
+                    if (i < tile_steps(x) &&
+                        mbar_test(bar(kBarKvFull + i % kTcStages), (i / kTcStages) & 1) &&
+                        (i < 2 || mbar_test(bar(kBarSFree + 2 * x + (i & 1)), ((i >> 1) - 1) & 1))) {
+                        ok = issue_s(x, i);
+                        next_s[x] = i + 1;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    t_last = global_timer_ns();
+                } else {
+                    __nanosleep(32);          // leave issue slots to the softmax warps of this sub-partition
+                    if (global_timer_ns() - t_last > p.timeout_ns) ok = false;
+                }
             }
-            if (ok) ok = issue_pv(nsteps - 1);
             if (!ok) atomicOr(p.status, kDevErrTimeout);
         }
         __syncwarp();
