@@ -9,19 +9,26 @@
 //
 // One CTA = two consecutive tiles A and B of 128 MMA rows each (queries x all
 // heads of one KV head, so every K/V tile in shared memory serves the whole
-// GQA group twice) of one chunk; keys advance 64 at a time (4 blocks) through a
-// 3-stage ring.  While one softmax warpgroup works on its tile, the tensor core
-// runs the other tile's products (ping-pong).
+// GQA group twice) of one chunk; keys advance 128 at a time (8 blocks).  A
+// kind::f16 MMA costs the tensor core about the same time for any N up to 128,
+// so both products run at N = 128: S = Q K^T over 128 keys and O += P V over
+// d = 128.  While one softmax warpgroup works on its tile, the tensor core runs
+// the other tile's products (ping-pong).
 //   warp 0       producer: bulk tensor copies (TMA, 128-byte swizzle) of each
-//                step's K and V blocks (16-bit caches), one lane per block
-//   warp 1       one lane issues tcgen05.mma: S_X(i) = Q_X K_i^T into a double
-//                buffer in tensor memory, then O_X += P_X(i-1) V_(i-1)
+//                step's K blocks and V blocks (16-bit caches) into separate
+//                2-stage rings, one lane per block
+//   warp 1       one lane issues tcgen05.mma: S_X(i) = Q_X K_i^T into tensor
+//                memory, O_X += P_X(i) V_i with P_X read from tensor memory
 //   warps 2-5    softmax of tile A, warps 6-9 softmax of tile B: one thread
 //                per row, S from tensor memory, causal mask, online max/sum,
-//                P to shared memory; O rescaled in tensor memory only when a
-//                row maximum grows by more than 2^8
+//                P (16-bit) written back over the columns of S it came from;
+//                O rescaled in tensor memory only when a row maximum grows by
+//                more than 2^8
 //   warps 10-13  FP8 caches only: gather e4m3 rows through the block table, widen
 //                them exactly to f16 and store them in the MMA layout
+// Per tile the chain is S(i) -> softmax(i) -> P.V(i) -> S(i+1): S(i+1) reuses
+// the columns P(i) sits in, and the tensor core runs one thread's MMAs in
+// order, so the completion of S(i+1) also means P.V(i) is done.
 // Every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -34,32 +41,32 @@ namespace pa {
 namespace {
 
 constexpr int kTcRows = 128;                 // MMA M of one tile
-constexpr int kTcKeys = 64;                  // keys per step (MMA N of S, K of PV)
+constexpr int kTcKeys = 128;                 // keys per step (MMA N of S, K of P.V)
 constexpr int kTcBlocksPerStep = kTcKeys / kBlockSize;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 2;
 constexpr uint32_t kQHalf = 16384;           // Q tile: [128 rows][64 elements] per d-half
-constexpr uint32_t kKvHalf = 8192;           // K or V of a step: [64 rows][64 elements] per d-half
+constexpr uint32_t kKvHalf = 16384;          // K or V of a step: [128 keys][64 elements] per d-half
+constexpr uint32_t kKvBytes = 2 * kKvHalf;
 constexpr uint32_t kOffQ = 0;                // Q_A, Q_B: 32 KiB each
-constexpr uint32_t kOffStage = 65536;        // stage s: K at +32768 s, V 16 KiB after it
-constexpr uint32_t kStageBytes = 32768;
-constexpr uint32_t kOffP = kOffStage + kTcStages * kStageBytes;   // P_A, P_B: [128 rows][64 keys]
-constexpr uint32_t kPBytes = 16384;
-constexpr uint32_t kOffBars = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffK = 65536;            // K stages, 32 KiB each
+constexpr uint32_t kOffV = kOffK + kTcStages * kKvBytes;      // V stages, 32 KiB each
+constexpr uint32_t kOffBars = kOffV + kTcStages * kKvBytes;
 constexpr uint32_t kBarBytes = 256;          // barriers + tensor-memory address
 constexpr uint32_t kOffCum = kOffBars + kBarBytes;
-constexpr uint32_t kTmemCols = 512;          // S_A 0,64  S_B 128,192  O_A 256  O_B 384
+constexpr uint32_t kTmemCols = 512;          // S_A/P_A 0  S_B/P_B 128  O_A 256  O_B 384
 constexpr float kRescaleLog2 = 8.0f;         // lazy rescale threshold (factor 256)
 
 // barrier indices (8 bytes each from kOffBars)
 enum {
-    kBarKvFull = 0,     // [3]
-    kBarKvEmpty = 3,    // [3]
-    kBarSFull = 6,      // [tile][2]
-    kBarSFree = 10,     // [tile][2]
-    kBarPFull = 14,     // [tile]
-    kBarPvDone = 16,    // [tile]
-    kBarQFull = 18,
-    kNumBars = 19
+    kBarKFull = 0,      // [stage]
+    kBarKEmpty = 2,     // [stage]
+    kBarVFull = 4,      // [stage]
+    kBarVEmpty = 6,     // [stage]
+    kBarSFull = 8,      // [tile]
+    kBarPFull = 10,     // [tile]
+    kBarPvDone = 12,    // [tile]
+    kBarQFull = 14,
+    kNumBars = 15
 };
 
 template <int Kind>
@@ -76,6 +83,28 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     ok = __shfl_sync(0xffffffffu, static_cast<int>(ok), 0) != 0;
     if (ok) mbar_try_wait(bar, parity);
     return ok;
+}
+
+// Three-input maximum / minimum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
 
 }  // namespace
@@ -103,14 +132,13 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(bar(kBarKvFull + s), kFp8 ? 4 : 1);
-            mbar_init(bar(kBarKvEmpty + s), 1);
+            mbar_init(bar(kBarKFull + s), kFp8 ? 4 : 1);
+            mbar_init(bar(kBarVFull + s), kFp8 ? 4 : 1);
+            mbar_init(bar(kBarKEmpty + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 1);
         }
         for (int x = 0; x < 2; ++x) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(bar(kBarSFull + 2 * x + b), 1);
-                mbar_init(bar(kBarSFree + 2 * x + b), 4);
-            }
+            mbar_init(bar(kBarSFull + x), 1);
             mbar_init(bar(kBarPFull + x), 4);
             mbar_init(bar(kBarPvDone + x), 1);
         }
@@ -197,12 +225,12 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    auto tS = [&](int x, int b) -> uint32_t { return tmem + 128u * x + 64u * b; };
+    auto tS = [&](int x) -> uint32_t { return tmem + 128u * x; };          // S, then P over its first 64 columns
     auto tO = [&](int x) -> uint32_t { return tmem + 256u + 128u * x; };
     bool ok = true;
 
     if (warp == 0) {
-        // ================= producer (16-bit caches): lane b < 4 copies block b of a step =================
+        // ================= producer (16-bit caches): lane b < 8 copies block b of a step =================
         if constexpr (!kFp8) {
             auto entry = [&](int i) -> int {
                 const int j = i * kTcBlocksPerStep + lane;
@@ -216,106 +244,109 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 }
                 return phys;
             };
-            int phys = entry(0);
-            for (int i = 0; i < nsteps && ok; ++i) {
-                const int st = i % kTcStages;
-                const int phys_next = i + 1 < nsteps ? entry(i + 1) : 0;
-                if (i >= kTcStages &&
-                    !warp_wait(bar(kBarKvEmpty + st), ((i / kTcStages) - 1) & 1, p.timeout_ns)) {
-                    if (lane == 0) atomicOr(p.status, kDevErrTimeout);
-                    ok = false;
-                    break;
-                }
-                const int nb = min(kTcBlocksPerStep, nblocks - i * kTcBlocksPerStep);
-                const uint32_t kdst = sbase + kOffStage + st * kStageBytes;
-                const uint32_t vdst = kdst + 2 * kKvHalf;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + st), static_cast<uint32_t>(nb) * 2 * 4096);
+            // block b -> rows 16b..16b+15 of each d-half of the stage
+            auto copy = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int nb, int phys) {
+                if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb) * 2 * 2048);
                 __syncwarp();
                 if (lane < nb) {
                     const int y = (phys * p.num_kv_heads + h) * kBlockSize;
-                    // block b -> rows 16b..16b+15 of each d-half
-                    tma_load_2d(kdst + lane * 2048, &kmap, 0, y, bar(kBarKvFull + st));
-                    tma_load_2d(kdst + kKvHalf + lane * 2048, &kmap, 64, y, bar(kBarKvFull + st));
-                    tma_load_2d(vdst + lane * 2048, &vmap, 0, y, bar(kBarKvFull + st));
-                    tma_load_2d(vdst + kKvHalf + lane * 2048, &vmap, 64, y, bar(kBarKvFull + st));
+                    tma_load_2d(dst + lane * 2048, map, 0, y, full);
+                    tma_load_2d(dst + kKvHalf + lane * 2048, map, 64, y, full);
                 }
+            };
+            int phys = entry(0);
+            for (int i = 0; i < nsteps && ok; ++i) {
+                const int st = i % kTcStages;
+                const uint32_t par = ((i / kTcStages) - 1) & 1;
+                const int phys_next = i + 1 < nsteps ? entry(i + 1) : 0;
+                const int nb = min(kTcBlocksPerStep, nblocks - i * kTcBlocksPerStep);
+                if (i >= kTcStages && !warp_wait(bar(kBarKEmpty + st), par, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                copy(&kmap, sbase + kOffK + st * kKvBytes, bar(kBarKFull + st), nb, phys);
+                if (i >= kTcStages && !warp_wait(bar(kBarVEmpty + st), par, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                copy(&vmap, sbase + kOffV + st * kKvBytes, bar(kBarVFull + st), nb, phys);
                 phys = phys_next;
             }
+            if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_f16<kMmaBf16>(kTcRows, kTcKeys, false);
             constexpr uint32_t idPV = umma_idesc_f16<kMmaBf16>(kTcRows, kHeadDim, true);
-            auto issue_s = [&](int x, int i) -> bool {
-                const int sb = i & 1;
-                if (i >= 2 && !mbar_wait_bounded(bar(kBarSFree + 2 * x + sb), ((i >> 1) - 1) & 1, p.timeout_ns))
-                    return false;
-                tc_fence_after();
+            auto issue_s = [&](int x, int i) {
                 const uint32_t qbase = sbase + kOffQ + x * 2 * kQHalf;
-                const uint32_t kbase = sbase + kOffStage + (i % kTcStages) * kStageBytes;
+                const uint32_t kbase = sbase + kOffK + (i % kTcStages) * kKvBytes;
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint64_t a = umma_desc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = umma_desc_sw128(kbase + (kk >> 2) * kKvHalf + (kk & 3) * 32, 16, 1024);
-                    umma_f16(tS(x, sb), a, b, idS, kk > 0 ? 1u : 0u);
+                    umma_f16(tS(x), a, b, idS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(kBarSFull + 2 * x + sb));
-                return true;
+                umma_commit(bar(kBarSFull + x));
             };
             auto issue_pv = [&](int x, int j) {
-                const uint32_t vbase = sbase + kOffStage + (j % kTcStages) * kStageBytes + 2 * kKvHalf;
-                const uint32_t pbase = sbase + kOffP + x * kPBytes;
+                const uint32_t vbase = sbase + kOffV + (j % kTcStages) * kKvBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    const uint64_t a = umma_desc_sw128(pbase + kk * 32, 16, 1024);
+                    // V is MN-major: d-halves kKvHalf apart, 16 keys = 2 KiB
                     const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
-                    umma_f16(tO(x), a, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(tO(x), tS(x) + 8 * kk, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(kBarPvDone + x));
             };
-            // Event loop: poll the barriers and issue whatever is ready, P.V first (it
-            // unblocks that tile's softmax), then the next S into a free buffer, so that
-            // one tile never waits behind the other.  No barrier can move past the
-            // phase tested here: each one's next phase needs an MMA not yet issued.
+            // Event loop: poll the barriers and issue whatever is ready, P.V first (the
+            // next S of that tile waits for it), then S.  No barrier tested here can run
+            // a phase ahead: each one's next phase needs an MMA not yet issued.
             const int zt = has_b ? 1 : 0;             // tile that zeroes V rows in the last step
             int next_s[2] = {0, 0}, next_pv[2] = {0, 0};
             ok = mbar_wait_bounded(bar(kBarQFull), 0, p.timeout_ns);
-            uint64_t t_last = global_timer_ns();
+            uint64_t t_last = 0;
+            uint32_t idle = 0;
             while (ok && (next_pv[0] < tile_steps(0) || next_pv[1] < tile_steps(1))) {
                 bool progress = false;
+#pragma unroll
                 for (int x = 0; x < 2; ++x) {
+                    const int other = 1 - x;
                     const int j = next_pv[x];
-                    if (j < tile_steps(x) && j < next_s[x] && mbar_test(bar(kBarPFull + x), j & 1)) {
+                    if (j < tile_steps(x) && j < next_s[x] && mbar_test(bar(kBarPFull + x), j & 1) &&
+                        mbar_test(bar(kBarVFull + j % kTcStages), (j / kTcStages) & 1)) {
                         // a 16-bit cache's last step also waits for the zeroing tile
+                        const int pv_zt = zt ? next_pv[1] : next_pv[0];
                         const bool blocked = !kFp8 && j == nsteps - 1 && x != zt && j < tile_steps(zt) &&
-                                             !(next_pv[zt] > j || mbar_test(bar(kBarPFull + zt), j & 1));
+                                             !(pv_zt > j || mbar_test(bar(kBarPFull + zt), j & 1));
                         if (!blocked) {
                             tc_fence_after();
                             issue_pv(x, j);
                             next_pv[x] = j + 1;
                             progress = true;
-                            const int other = 1 - x;
                             if (j >= tile_steps(other) || next_pv[other] > j)
-                                umma_commit(bar(kBarKvEmpty + (j % kTcStages)));   // both tiles done with stage
+                                umma_commit(bar(kBarVEmpty + j % kTcStages));   // both tiles done with V_j
+                            if (j + 1 == tile_steps(x)) umma_commit(bar(kBarPvDone + x));
                         }
                     }
-                }
-                for (int x = 0; x < 2; ++x) {
+                    // this tile's next S right behind its P.V, ahead of the other tile's work
                     const int i = next_s[x];
-                    if (i < tile_steps(x) &&
-                        mbar_test(bar(kBarKvFull + i % kTcStages), (i / kTcStages) & 1) &&
-                        (i < 2 || mbar_test(bar(kBarSFree + 2 * x + (i & 1)), ((i >> 1) - 1) & 1))) {
-                        ok = issue_s(x, i);
+                    if (i < tile_steps(x) && next_pv[x] >= i &&
+                        mbar_test(bar(kBarKFull + i % kTcStages), (i / kTcStages) & 1)) {
+                        tc_fence_after();
+                        issue_s(x, i);
                         next_s[x] = i + 1;
                         progress = true;
+                        if (i >= tile_steps(other) || next_s[other] > i)
+                            umma_commit(bar(kBarKEmpty + i % kTcStages));       // both tiles done with K_i
                     }
                 }
                 if (progress) {
+                    idle = 0;
+                } else if (++idle == 1) {
                     t_last = global_timer_ns();
-                } else {
-                    __nanosleep(32);          // leave issue slots to the softmax warps of this sub-partition
-                    if (global_timer_ns() - t_last > p.timeout_ns) ok = false;
+                } else if ((idle & 255) == 0 && global_timer_ns() - t_last > p.timeout_ns) {
+                    ok = false;
                 }
             }
             if (!ok) atomicOr(p.status, kDevErrTimeout);
@@ -360,10 +391,10 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         const float vscale = kFp8 ? __ldg(p.v_scale) : 1.0f;
         const float s_log2 = p.scale_log2 * kscale;
         const bool pos_scale = s_log2 >= 0.f;
+        const uint32_t s_addr = tS(x) + lane_off;
         float m_used = -INFINITY, l = 0.f;
         for (int i = 0; i < steps && ok; ++i) {
-            const int sb = i & 1;
-            if (!warp_wait(bar(kBarSFull + 2 * x + sb), (i >> 1) & 1, p.timeout_ns)) {
+            if (!warp_wait(bar(kBarSFull + x), i & 1, p.timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -371,114 +402,121 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             const int key0 = i * kTcKeys;
             const bool need_mask = key0 + kTcKeys - 1 > pos_first;
             const int lim = pos - key0;                 // columns > lim are masked
-            const uint32_t s_addr = tS(x, sb) + lane_off;
-            // pass 1: row maximum of the raw scores (scale > 0 keeps the order, < 0 reverses it)
-            float hi = -INFINITY, lo = INFINITY;
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 32; ++c) {
-                uint32_t sv[32];
-                tmem_ld32(s_addr + 32 * c, sv);
-                tmem_wait_ld();
-                if (!need_mask) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        hi = fmaxf(hi, __uint_as_float(sv[e]));
-                        lo = fminf(lo, __uint_as_float(sv[e]));
-                    }
+            // pass 1: row maximum of s * scale = max(s) * scale for scale >= 0, min(s) * scale
+            // otherwise; four independent chains, masked columns only on diagonal steps
+            float mx;
+            if (!need_mask) {
+                float e4[4];
+                if (pos_scale) {
+                    e4[0] = e4[1] = e4[2] = e4[3] = -INFINITY;
                 } else {
+                    e4[0] = e4[1] = e4[2] = e4[3] = INFINITY;
+                }
+#pragma unroll 1
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t sv[64];
+                    tmem_ld32(s_addr + 64 * h2, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                    tmem_ld32(s_addr + 64 * h2 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                    tmem_wait_ld();
+                    if (pos_scale) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const bool keep = 32 * c + e <= lim;
-                        hi = fmaxf(hi, keep ? __uint_as_float(sv[e]) : -INFINITY);
-                        lo = fminf(lo, keep ? __uint_as_float(sv[e]) : INFINITY);
+                        for (int e = 0; e < 64; e += 2)
+                            e4[(e >> 1) & 3] = max3f(e4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2)
+                            e4[(e >> 1) & 3] = min3f(e4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
                     }
                 }
+                mx = (pos_scale ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
+                                : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]))) * s_log2;
+            } else {
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                for (int c = 0; c < kTcKeys / 32; ++c) {
+                    uint32_t sv[32];
+                    tmem_ld32(s_addr + 32 * c, sv);
+                    tmem_wait_ld();
+                    const int lc = lim - 32 * c;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float v = __uint_as_float(sv[e]) * s_log2;
+                        mx4[e & 3] = fmaxf(mx4[e & 3], e <= lc ? v : -INFINITY);
+                    }
+                }
+                mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));   // -inf when every column is masked
             }
-            const float mx = (pos_scale ? hi : lo) * s_log2;   // -inf when every column is masked
             const bool need = mx > m_used + kRescaleLog2;
             const bool resc = __any_sync(0xffffffffu, need);
             const float m_new = need ? fmaxf(m_used, mx) : m_used;
             const float alpha = ex2_approx(m_used - m_new);    // 0 on the first step, 1 when kept
             m_used = m_new;
-            // P buffer and O are busy until this tile's previous P.V is done
-            if (i >= 1) {
-                if (!warp_wait(bar(kBarPvDone + x), (i - 1) & 1, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (resc) {
+            // O is final for P.V(i-1): S(i) was issued after it and completes after it
+            if (i >= 1 && resc) {
 #pragma unroll 1
-                    for (int c = 0; c < kHeadDim / 32; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO(x) + lane_off + 32 * c, ov);
-                        tmem_wait_ld();
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO(x) + lane_off + 32 * c, ov);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(tO(x) + lane_off + 32 * c, ov);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(tO(x) + lane_off + 32 * c, ov);
                 }
             }
-            // pass 2: p = 2^(s * scale - m), stored as the A operand of P.V
-            float sum = 0.f;
+            // pass 2: p = 2^(s * scale - m) as the 16-bit A operand of P.V, written over
+            // S columns already read (keys 32 c .. +31 -> columns 16 c .. +15)
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
             const float neg_m = -m_new;
-            uint8_t* prow = sm + kOffP + x * kPBytes;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < kTcKeys / 32; ++c) {
                 uint32_t sv[32];
                 tmem_ld32(s_addr + 32 * c, sv);
                 tmem_wait_ld();
+                uint32_t pw[16];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = 8 * q4 + 2 * k;
-                        float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), s_log2, neg_m));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), s_log2, neg_m));
-                        if (need_mask) {
-                            p0 = 32 * c + e <= lim ? p0 : 0.f;
-                            p1 = 32 * c + e + 1 <= lim ? p1 : 0.f;
-                        }
-                        sum += p0 + p1;
-                        w[k] = pack2<kMmaBf16>(p0, p1);
+                for (int e = 0; e < 32; e += 2) {
+                    float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), s_log2, neg_m));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), s_log2, neg_m));
+                    if (need_mask) {
+                        p0 = 32 * c + e <= lim ? p0 : 0.f;
+                        p1 = 32 * c + e + 1 <= lim ? p1 : 0.f;
                     }
-                    *reinterpret_cast<uint4*>(prow + sw128_offset(r, (4 * c + q4) * 8)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                    sum4[(e >> 1) & 3] += p0 + p1;
+                    pw[e >> 1] = pack2<kMmaBf16>(p0, p1);
                 }
+                tmem_st16(s_addr + 16 * c, pw);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSFree + 2 * x + sb));
-            l = l * alpha + sum;
+            tmem_wait_st();
+            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            bool zeroed = false;
             if constexpr (!kFp8) {
                 // keys past the CTA's last position get P = 0, but their V rows hold unloaded
                 // (stale) or poisoned bytes and 0 x NaN is NaN: the last tile zeroes them
                 if (i == nsteps - 1 && x == (has_b ? 1 : 0)) {
                     const int st = i % kTcStages;
-                    if (!warp_wait(bar(kBarKvFull + st), (i / kTcStages) & 1, p.timeout_ns)) {
+                    if (!warp_wait(bar(kBarVFull + st), (i / kTcStages) & 1, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    if (r < kTcKeys && key0 + r > pos_last_cta) {
-                        uint8_t* vrow = sm + kOffStage + st * kStageBytes + 2 * kKvHalf + r * 128;
+                    if (key0 + r > pos_last_cta) {
+                        uint8_t* vrow = sm + kOffV + st * kKvBytes + r * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
                             *reinterpret_cast<uint4*>(vrow + kKvHalf + 16 * c) = make_uint4(0, 0, 0, 0);
                         }
                     }
+                    zeroed = true;
                 }
             }
-            fence_proxy_async_smem();
+            if (zeroed) fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPFull + x));
         }
         // ---- epilogue: O / l ----
         if (steps > 0) {
-            if (ok && warp_wait(bar(kBarPvDone + x), (steps - 1) & 1, p.timeout_ns)) {
+            if (ok && warp_wait(bar(kBarPvDone + x), 0, p.timeout_ns)) {
                 tc_fence_after();
                 const float inv = vscale / l;
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow);
@@ -504,15 +542,16 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             }
         }
     } else if constexpr (kFp8) {
-        // ================= FP8 converters: thread = half a key row (64 d) of the step =================
+        // ================= FP8 converters =================
+        // A step's K (and its V) is two items of 64 keys; thread = half a key row
+        // (64 d) of an item.  Items are fetched two ahead, in the order
+        // K(i) 0, K(i) 1, V(i) 0, V(i) 1, K(i+1) 0, ...
         const int c = threadIdx.x - 10 * 32;           // 0..127
-        const int krow = c >> 1;                       // key within the step
+        const int krow = c >> 1;                       // key within the item
         const int half = c & 1;                        // d-half
-        const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
-        const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
-        auto load_row = [&](int i, uint4 (&kx)[4], uint4 (&vx)[4]) {
-            const int key = i * kTcKeys + krow;
-            if (key <= pos_last_cta) {      // later keys get P = 0: store zeros
+        auto load_item = [&](const uint8_t* cache, int i, int u, uint4 (&x4)[4]) {
+            const int key = i * kTcKeys + 64 * u + krow;
+            if (i < nsteps && key <= pos_last_cta) {      // later keys get P = 0: store zeros
                 int phys = __ldg(bt + (key >> 4));
                 if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
                     atomicOr(p.status, kDevErrRange);
@@ -520,20 +559,17 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 }
                 const size_t off =
                     ((static_cast<size_t>(phys) * p.num_kv_heads + h) * kBlockSize + (key & 15)) * kHeadDim + 64 * half;
-                const uint4* ks = reinterpret_cast<const uint4*>(kc + off);
-                const uint4* vs = reinterpret_cast<const uint4*>(vc + off);
+                const uint4* src = reinterpret_cast<const uint4*>(cache + off);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kx[e] = __ldg(ks + e);
-                    vx[e] = __ldg(vs + e);
-                }
+                for (int e = 0; e < 4; ++e) x4[e] = __ldg(src + e);
             } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) kx[e] = vx[e] = make_uint4(0, 0, 0, 0);
+                for (int e = 0; e < 4; ++e) x4[e] = make_uint4(0, 0, 0, 0);
             }
         };
-        auto widen_store = [&](uint8_t* dst, const uint4 (&x4)[4]) {
+        auto widen_store = [&](uint8_t* stage, int u, const uint4 (&x4)[4]) {
             // 64 e4m3 codes (d = 64 half + 16e ..) -> exact f16, 128-byte swizzle
+            const int row = 64 * u + krow;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const uint32_t w[4] = {x4[e].x, x4[e].y, x4[e].z, x4[e].w};
@@ -543,33 +579,44 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     f[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
                     f[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
                 }
-                *reinterpret_cast<uint4*>(dst + half * kKvHalf + sw128_offset(krow, 16 * e)) =
+                *reinterpret_cast<uint4*>(stage + half * kKvHalf + sw128_offset(row, 16 * e)) =
                     make_uint4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<uint4*>(dst + half * kKvHalf + sw128_offset(krow, 16 * e + 8)) =
+                *reinterpret_cast<uint4*>(stage + half * kKvHalf + sw128_offset(row, 16 * e + 8)) =
                     make_uint4(f[4], f[5], f[6], f[7]);
             }
         };
-        uint4 kx[4], vx[4], kn[4], vn[4];
-        load_row(0, kx, vx);
+        const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
+        const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
+        uint4 xa[4], xb[4];
+        load_item(kc, 0, 0, xa);
+        load_item(kc, 0, 1, xb);
         for (int i = 0; i < nsteps && ok; ++i) {
             const int st = i % kTcStages;
-            if (i + 1 < nsteps) load_row(i + 1, kn, vn);          // in flight while this step converts
-            if (i >= kTcStages &&
-                !warp_wait(bar(kBarKvEmpty + st), ((i / kTcStages) - 1) & 1, p.timeout_ns)) {
+            const uint32_t par = ((i / kTcStages) - 1) & 1;
+            if (i >= kTcStages && !warp_wait(bar(kBarKEmpty + st), par, p.timeout_ns)) {
                 ok = false;
                 break;
             }
-            uint8_t* kdst = sm + kOffStage + st * kStageBytes;
-            widen_store(kdst, kx);
-            widen_store(kdst + 2 * kKvHalf, vx);
+            uint8_t* kdst = sm + kOffK + st * kKvBytes;
+            widen_store(kdst, 0, xa);
+            load_item(vc, i, 0, xa);
+            widen_store(kdst, 1, xb);
+            load_item(vc, i, 1, xb);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarKvFull + st));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                kx[e] = kn[e];
-                vx[e] = vn[e];
+            if (lane == 0) mbar_arrive(bar(kBarKFull + st));
+            if (i >= kTcStages && !warp_wait(bar(kBarVEmpty + st), par, p.timeout_ns)) {
+                ok = false;
+                break;
             }
+            uint8_t* vdst = sm + kOffV + st * kKvBytes;
+            widen_store(vdst, 0, xa);
+            load_item(kc, i + 1, 0, xa);
+            widen_store(vdst, 1, xb);
+            load_item(kc, i + 1, 1, xb);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarVFull + st));
         }
         if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
     }
