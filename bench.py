@@ -9,9 +9,10 @@ CUDA graph.  Inputs are resident in HBM before timing starts.
 Printed (rank 0, one JSON line): KV GB/s = algorithmic K/V bytes the step must
 read (every cached token of every sequence, every KV head, every layer) divided
 by the step time; also sequence-steps/s, the fraction of HBM peak, the
-roofline of the decode kernel, an end-to-end number through the public API
-with host buffers, clocks seen during the timed region, and the CPU oracle's
-throughput on a bounded sample of the same workload.
+roofline of the dominant kernel (decode; the chunk kernel for a mixed batch),
+an end-to-end number through the public API with host buffers, clocks seen
+during the timed region, and the CPU oracle's throughput on a bounded sample of
+the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 """
@@ -38,6 +39,7 @@ from paged_kv_cache_99_gb300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and seq-steps/sec"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 DEFAULT_WORKLOAD = "qwen2.5-1.5b"
 DESCRIPTIONS = {
     "tiny": "tiny decode: 1 layer, B=4, seq_lens 8/17/31/46, H_q=8, H_kv=2, d=128, block 16, bf16",
@@ -55,6 +57,28 @@ ELEM = {"bf16": 2, "fp16": 2, "fp8": 1}
 def kv_read_bytes(w: W.Workload) -> int:
     """Algorithmic K/V bytes of one step: 2 * H_kv * d * b per cached token, per layer."""
     return w.num_layers * int(w.seq_lens.sum().item()) * 2 * w.num_kv_heads * w.head_dim * ELEM[w.cache_dtype]
+
+
+def chunk_flops(w: W.Workload) -> int:
+    """Algorithmic FLOPs of the prefill chunks of one layer: QK^T and PV, 2 per
+    multiply-add, over the causal key range of every chunk row (no padding)."""
+    ql = (w.query_start_loc[1:] - w.query_start_loc[:-1]).tolist()
+    n = w.seq_lens.tolist()
+    keys = sum(q * (n_s - q) + q * (q + 1) // 2 for q, n_s in zip(ql, n) if q > 1)
+    return 4 * w.head_dim * w.num_q_heads * keys
+
+
+def chunk_subbatch(w: W.Workload, layer: int = 0):
+    """The chunk rows (q_len > 1) of a mixed batch as a batch of their own."""
+    ql = (w.query_start_loc[1:] - w.query_start_loc[:-1]).tolist()
+    idx = [i for i, q in enumerate(ql) if q > 1]
+    starts = [0]
+    for i in idx:
+        starts.append(starts[-1] + ql[i])
+    dev = w.q[layer].device
+    q = torch.cat([w.q[layer][int(w.query_start_loc[i]):int(w.query_start_loc[i + 1])] for i in idx])
+    qsl = torch.tensor(starts, dtype=torch.int32, device=dev)
+    return q, qsl, w.block_tables[idx].contiguous(), w.seq_lens[idx].contiguous(), max(ql[i] for i in idx)
 
 
 def dist_env():
@@ -200,7 +224,8 @@ def run_ours(args, rank, world, local):
     kv_bytes = kv_read_bytes(w)
     step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches))
     decode_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, decode_only_kernels=True))
-    launches_per_step = w.num_layers * (2 if w.num_new_tokens else 1)
+    # per layer: the slot write, the attention kernel and its combine, the chunk kernel of a mixed batch
+    launches_per_step = w.num_layers * ((1 if w.num_new_tokens else 0) + 2 + (0 if w.is_decode_only else 1))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     unique_bytes = sum(c.numel() * c.element_size() * 2 for c in w.k_cache)
     flush = unique_bytes < 2 * l2
@@ -249,6 +274,28 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     dec_ms = sum(a.elapsed_time(b) for a, b in dg_ev) / args.steps / w.num_layers
 
+    # ---- a mixed batch is dominated by the chunk kernel: time it on the chunk rows alone ----
+    chunk = None
+    if not w.is_decode_only:
+        cq, cqsl, cbt, csl, cmax = chunk_subbatch(w)
+        cws = pa.new_workspace(int(csl.numel()), w.num_q_heads, w.num_kv_heads, device=dev)
+        cout = torch.empty_like(cq)
+        kc, vc = layers_caches[0]
+        ks = w.k_scale[0:1] if w.k_scale is not None else None
+        vs = w.v_scale[0:1] if w.v_scale is not None else None
+        cg = capture(lambda: pa.pa_mixed(cout, cq, cqsl, kc, vc, cbt, csl, cmax, w.scale, cws, ks, vs))
+        for _ in range(3):
+            cg.replay()
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            if flush:
+                flush_buf.fill_(1)
+            cev[i][0].record()
+            cg.replay()
+            cev[i][1].record()
+        torch.cuda.synchronize()
+        chunk = (sum(a.elapsed_time(b) for a, b in cev) / args.steps, chunk_flops(w))
+
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, w, pa, ws, outs, layers_caches, dev) if not args.no_e2e else None
 
@@ -286,7 +333,7 @@ def run_ours(args, rank, world, local):
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / hbm_peak, 2),
         "roofline": {
-            "kernel": "pa_decode" if w.is_decode_only else "pa_mixed decode rows",
+            "kernel": "pa_decode",
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": hbm_peak,
@@ -302,6 +349,25 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
     }
+    if chunk is not None:
+        # the tensor-core chunk kernel dominates a mixed step: its roofline is the reported one,
+        # against the measured dense bf16 rate (f16 runs at the same nominal rate)
+        c_ms, c_flops = chunk
+        tpeak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+        c_achieved = c_flops / (c_ms * 1e-3) / 1e12
+        line["roofline_decode_rows"] = dict(line["roofline"], kernel="pa_mixed (decode rows and chunks)")
+        line["roofline"] = {
+            "kernel": "chunk_tc (pa_mixed on the chunk rows alone)",
+            "bound": "tensor",
+            "achieved": round(c_achieved, 2),
+            "peak": tpeak,
+            "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)" if peak_src == "measured" else "fallback",
+            "unit": "TFLOP/s",
+            "frac": round(c_achieved / tpeak, 4),
+            "traffic": None,
+            "algorithmic_flops_per_launch": c_flops,
+            "avg_launch_ms": round(c_ms, 5),
+        }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         line["cpu_baseline"]["kv_bytes_per_step"] = kv_bytes

@@ -20,12 +20,13 @@
 //   warp 1       one lane issues tcgen05.mma: S_X(i) = Q_X K_i^T into tensor
 //                memory, O_X += P_X(i) V_i with P_X read from tensor memory
 //   warps 2-5    softmax of tile A, warps 6-9 softmax of tile B: one thread
-//                per row, S from tensor memory, causal mask, online max/sum,
-//                P (16-bit) written back over the columns of S it came from;
-//                O rescaled in tensor memory only when a row maximum grows by
-//                more than 2^8
-//   warps 10-13  FP8 caches only: gather e4m3 rows through the block table, widen
-//                them exactly to f16 and store them in the MMA layout
+//                per row holds its 128 scores in registers (one tensor-memory
+//                read per step), causal mask, online max/sum, P (16-bit)
+//                written back over the columns of S; O rescaled in tensor
+//                memory only when a row maximum grows by more than 2^8
+//   warps 0, 10  FP8 caches only (in place of the producer): gather e4m3 rows
+//                through the block table, widen them exactly to f16 and store
+//                them in the MMA layout
 // Per tile the chain is S(i) -> softmax(i) -> P.V(i) -> S(i+1): S(i+1) reuses
 // the columns P(i) sits in, and the tensor core runs one thread's MMAs in
 // order, so the completion of S(i+1) also means P.V(i) is done.
@@ -73,7 +74,7 @@ template <int Kind>
 struct TcCfg {
     static constexpr bool kFp8 = Kind == kKindFp8;
     static constexpr bool kMmaBf16 = Kind == kKindBf16;
-    static constexpr int kWarps = kFp8 ? 14 : 10;
+    static constexpr int kWarps = kFp8 ? 11 : 10;
 };
 
 // Bounded wait by lane 0 of the warp, then an acquire by every lane.
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(bar(kBarKFull + s), kFp8 ? 4 : 1);
-            mbar_init(bar(kBarVFull + s), kFp8 ? 4 : 1);
+            mbar_init(bar(kBarKFull + s), kFp8 ? 2 : 1);
+            mbar_init(bar(kBarVFull + s), kFp8 ? 2 : 1);
             mbar_init(bar(kBarKEmpty + s), 1);
             mbar_init(bar(kBarVEmpty + s), 1);
         }
@@ -229,9 +230,9 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     auto tO = [&](int x) -> uint32_t { return tmem + 256u + 128u * x; };
     bool ok = true;
 
-    if (warp == 0) {
+    if (!kFp8 && warp == 0) {
         // ================= producer (16-bit caches): lane b < 8 copies block b of a step =================
-        if constexpr (!kFp8) {
+        {
             auto entry = [&](int i) -> int {
                 const int j = i * kTcBlocksPerStep + lane;
                 int phys = 0;
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             if (!ok) atomicOr(p.status, kDevErrTimeout);
         }
         __syncwarp();
-    } else if (warp < 10) {
+    } else if (warp >= 2 && warp < 10) {
         // ================= softmax: warps 2-5 tile A, 6-9 tile B; thread = one MMA row =================
         const int x = warp < 6 ? 0 : 1;
         const int quarter = warp & 3;                  // tensor-memory lanes 32 quarter .. + 31
@@ -402,48 +403,35 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             const int key0 = i * kTcKeys;
             const bool need_mask = key0 + kTcKeys - 1 > pos_first;
             const int lim = pos - key0;                 // columns > lim are masked
-            // pass 1: row maximum of s * scale = max(s) * scale for scale >= 0, min(s) * scale
+            // the whole row of S in registers: one tensor-memory round trip per step
+            uint32_t sv[kTcKeys];
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 32; ++c)
+                tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+            tmem_wait_ld();
+            // row maximum of s * scale = max(s) * scale for scale >= 0, min(s) * scale
             // otherwise; four independent chains, masked columns only on diagonal steps
             float mx;
             if (!need_mask) {
                 float e4[4];
                 if (pos_scale) {
                     e4[0] = e4[1] = e4[2] = e4[3] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < kTcKeys; e += 2)
+                        e4[(e >> 1) & 3] = max3f(e4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                    mx = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3])) * s_log2;
                 } else {
                     e4[0] = e4[1] = e4[2] = e4[3] = INFINITY;
-                }
-#pragma unroll 1
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t sv[64];
-                    tmem_ld32(s_addr + 64 * h2, *reinterpret_cast<uint32_t(*)[32]>(sv));
-                    tmem_ld32(s_addr + 64 * h2 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-                    tmem_wait_ld();
-                    if (pos_scale) {
 #pragma unroll
-                        for (int e = 0; e < 64; e += 2)
-                            e4[(e >> 1) & 3] = max3f(e4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 64; e += 2)
-                            e4[(e >> 1) & 3] = min3f(e4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-                    }
+                    for (int e = 0; e < kTcKeys; e += 2)
+                        e4[(e >> 1) & 3] = min3f(e4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                    mx = fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3])) * s_log2;
                 }
-                mx = (pos_scale ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
-                                : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]))) * s_log2;
             } else {
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-                for (int c = 0; c < kTcKeys / 32; ++c) {
-                    uint32_t sv[32];
-                    tmem_ld32(s_addr + 32 * c, sv);
-                    tmem_wait_ld();
-                    const int lc = lim - 32 * c;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float v = __uint_as_float(sv[e]) * s_log2;
-                        mx4[e & 3] = fmaxf(mx4[e & 3], e <= lc ? v : -INFINITY);
-                    }
-                }
+                for (int e = 0; e < kTcKeys; ++e)
+                    mx4[e & 3] = fmaxf(mx4[e & 3], e <= lim ? __uint_as_float(sv[e]) * s_log2 : -INFINITY);
                 mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));   // -inf when every column is masked
             }
             const bool need = mx > m_used + kRescaleLog2;
@@ -451,6 +439,27 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             const float m_new = need ? fmaxf(m_used, mx) : m_used;
             const float alpha = ex2_approx(m_used - m_new);    // 0 on the first step, 1 when kept
             m_used = m_new;
+            // p = 2^(s * scale - m) as the 16-bit A operand of P.V, written over the
+            // columns of S (keys 32 c .. +31 -> columns 16 c .. +15)
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            const float neg_m = -m_new;
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 32; ++c) {
+                uint32_t pw[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int k = 32 * c + e;
+                    float p0 = ex2_approx(fmaf(__uint_as_float(sv[k]), s_log2, neg_m));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(sv[k + 1]), s_log2, neg_m));
+                    if (need_mask) {
+                        p0 = k <= lim ? p0 : 0.f;
+                        p1 = k + 1 <= lim ? p1 : 0.f;
+                    }
+                    sum4[(e >> 1) & 3] += p0 + p1;
+                    pw[e >> 1] = pack2<kMmaBf16>(p0, p1);
+                }
+                tmem_st16(s_addr + 16 * c, pw);
+            }
             // O is final for P.V(i-1): S(i) was issued after it and completes after it
             if (i >= 1 && resc) {
 #pragma unroll 1
@@ -462,29 +471,6 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
                     tmem_st32(tO(x) + lane_off + 32 * c, ov);
                 }
-            }
-            // pass 2: p = 2^(s * scale - m) as the 16-bit A operand of P.V, written over
-            // S columns already read (keys 32 c .. +31 -> columns 16 c .. +15)
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-            const float neg_m = -m_new;
-#pragma unroll 1
-            for (int c = 0; c < kTcKeys / 32; ++c) {
-                uint32_t sv[32];
-                tmem_ld32(s_addr + 32 * c, sv);
-                tmem_wait_ld();
-                uint32_t pw[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), s_log2, neg_m));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), s_log2, neg_m));
-                    if (need_mask) {
-                        p0 = 32 * c + e <= lim ? p0 : 0.f;
-                        p1 = 32 * c + e + 1 <= lim ? p1 : 0.f;
-                    }
-                    sum4[(e >> 1) & 3] += p0 + p1;
-                    pw[e >> 1] = pack2<kMmaBf16>(p0, p1);
-                }
-                tmem_st16(s_addr + 16 * c, pw);
             }
             tmem_wait_st();
             l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
@@ -542,14 +528,12 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             }
         }
     } else if constexpr (kFp8) {
-        // ================= FP8 converters =================
-        // A step's K (and its V) is two items of 64 keys; thread = half a key row
-        // (64 d) of an item.  Items are fetched two ahead, in the order
-        // K(i) 0, K(i) 1, V(i) 0, V(i) 1, K(i+1) 0, ...
-        const int c = threadIdx.x - 10 * 32;           // 0..127
-        const int krow = c >> 1;                       // key within the item
-        const int half = c & 1;                        // d-half
-        auto load_item = [&](const uint8_t* cache, int i, int u, uint4 (&x4)[4]) {
+        // ================= FP8 converters: warps 0 and 10 =================
+        // A step's K (and its V) is two items of 64 keys; thread = one key row (128 d)
+        // of an item.  Items are fetched two ahead, in the order K(i) 0, K(i) 1,
+        // V(i) 0, V(i) 1, K(i+1) 0, ...
+        const int krow = warp == 0 ? lane : 32 + lane;     // key within the item
+        auto load_item = [&](const uint8_t* cache, int i, int u, uint4 (&x8)[8]) {
             const int key = i * kTcKeys + 64 * u + krow;
             if (i < nsteps && key <= pos_last_cta) {      // later keys get P = 0: store zeros
                 int phys = __ldg(bt + (key >> 4));
@@ -557,37 +541,35 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     atomicOr(p.status, kDevErrRange);
                     phys = 0;
                 }
-                const size_t off =
-                    ((static_cast<size_t>(phys) * p.num_kv_heads + h) * kBlockSize + (key & 15)) * kHeadDim + 64 * half;
+                const size_t off = ((static_cast<size_t>(phys) * p.num_kv_heads + h) * kBlockSize + (key & 15)) * kHeadDim;
                 const uint4* src = reinterpret_cast<const uint4*>(cache + off);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) x4[e] = __ldg(src + e);
+                for (int e = 0; e < 8; ++e) x8[e] = __ldg(src + e);
             } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) x4[e] = make_uint4(0, 0, 0, 0);
+                for (int e = 0; e < 8; ++e) x8[e] = make_uint4(0, 0, 0, 0);
             }
         };
-        auto widen_store = [&](uint8_t* stage, int u, const uint4 (&x4)[4]) {
-            // 64 e4m3 codes (d = 64 half + 16e ..) -> exact f16, 128-byte swizzle
+        auto widen_store = [&](uint8_t* stage, int u, const uint4 (&x8)[8]) {
+            // 128 e4m3 codes -> exact f16, two d-halves, 128-byte swizzle
             const int row = 64 * u + krow;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t w[4] = {x4[e].x, x4[e].y, x4[e].z, x4[e].w};
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t w[4] = {x8[e].x, x8[e].y, x8[e].z, x8[e].w};
                 uint32_t f[8];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     f[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
                     f[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
                 }
-                *reinterpret_cast<uint4*>(stage + half * kKvHalf + sw128_offset(row, 16 * e)) =
-                    make_uint4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<uint4*>(stage + half * kKvHalf + sw128_offset(row, 16 * e + 8)) =
-                    make_uint4(f[4], f[5], f[6], f[7]);
+                uint8_t* dst = stage + (e >> 2) * kKvHalf;
+                *reinterpret_cast<uint4*>(dst + sw128_offset(row, 16 * (e & 3))) = make_uint4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<uint4*>(dst + sw128_offset(row, 16 * (e & 3) + 8)) = make_uint4(f[4], f[5], f[6], f[7]);
             }
         };
         const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
         const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
-        uint4 xa[4], xb[4];
+        uint4 xa[8], xb[8];
         load_item(kc, 0, 0, xa);
         load_item(kc, 0, 1, xb);
         for (int i = 0; i < nsteps && ok; ++i) {

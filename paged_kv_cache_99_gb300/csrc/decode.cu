@@ -81,9 +81,7 @@ __device__ __forceinline__ T shfl(T v, int src) {
 }  // namespace
 
 template <int Kind, bool QBf16>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
-    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  const DecodeParams p) {
+__device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p) {
     using Cfg = DecodeCfg<Kind>;
     constexpr bool kFp8 = Cfg::kFp8;
     constexpr bool kMmaBf16 = Kind == kKindBf16;   // fp16 and FP8 (widened) use f16 MMA
@@ -113,7 +111,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
         tmap_prefetch(&vmap);
     }
 
-    grid_dependency_wait();
+    if (!p.overlap_prior) grid_dependency_wait();
 
     const int B = p.num_seqs;
     const int UH = p.num_kv_heads * p.head_groups;
@@ -471,6 +469,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
         }
         cursor_advance(C, cum, B, UH);
     }
+}
+
+template <int Kind, bool QBf16>
+__global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const DecodeParams p) {
+    decode_body<Kind, QBf16>(kmap, vmap, p);
+    // Overlapping a chunk launch of the same call (which neither reads what this grid
+    // writes nor writes what it reads): the last CTA alone waits for it before exiting,
+    // so that this grid, and the combine chained behind it, completes after it while
+    // every other CTA frees its SM as soon as its range is done.
+    if (p.overlap_prior && blockIdx.x == gridDim.x - 1) grid_dependency_wait();
 }
 
 // Log-sum-exp combine of the units split across workers:

@@ -152,7 +152,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
                       const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads, float scale,
                       pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
                       void* workspace, size_t workspace_bytes, int num_workers, int num_blocks,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool overlap_prior = false) {
     int dev = 0;
     DeviceState* st = device_state(&dev);
     if (!st) return PA_ERR_CUDA;
@@ -214,6 +214,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = num_blocks;
     p.num_workers = W;
+    p.overlap_prior = overlap_prior ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
@@ -420,7 +421,8 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
     if (!query_start_loc || total_q < 0 || max_q_len < 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_q == 0) return PA_OK;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (max_q_len >= 2) {
+    const bool chunks = max_q_len >= 2;
+    if (chunks) {
         const CacheKind kind = kind_of(cache_dtype);
         CUtensorMap kmap, vmap;
         s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, kind == kKindFp8);
@@ -432,9 +434,12 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
                        v_scale, workspace, cs);
         if (s != PA_OK) return s;
     }
+    // the decode rows stream K/V while the chunk tiles keep the tensor cores busy: the
+    // decode grid starts once every chunk CTA is resident and fills the SMs the
+    // chunk grid leaves idle
     return decode_impl(out, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                        num_seqs, num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale,
-                       workspace, workspace_bytes, 0, num_blocks, cs);
+                       workspace, workspace_bytes, 0, num_blocks, cs, chunks);
 }
 
 pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -46,6 +46,9 @@ struct DecodeParams {
     int max_blocks;                   // block-table row length
     int num_blocks;                   // pool size
     int num_workers;                  // warps taking part
+    int overlap_prior;                // nonzero: the previous launch is this call's chunk kernel,
+                                      // which started only after its own predecessors finished;
+                                      // run beside it and wait for it only before exiting
     float scale_log2;                 // softmax scale * log2(e)
     unsigned long long timeout_ns;    // bound of every barrier wait
 };
