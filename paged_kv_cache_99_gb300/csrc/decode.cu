@@ -73,6 +73,18 @@ __device__ __forceinline__ int worker_of(long long f, long long T, int W) {
     return static_cast<int>(((f + 1) * W - 1) / T);
 }
 
+// Decode rows of a mixed batch are the sequences with q_len == 1.
+__device__ __forceinline__ bool decode_row(const DecodeParams& p, int s) {
+    return p.query_start_loc == nullptr || p.query_start_loc[s + 1] - p.query_start_loc[s] == 1;
+}
+
+// Blocks sequence s contributes to the flattened order (its blocks x units).
+__device__ __forceinline__ int unit_blocks_of(const DecodeParams& p, int s, int UH) {
+    if (!decode_row(p, s)) return 0;
+    const int nb = (max(p.seq_lens[s], 0) + kBlockSize - 1) / kBlockSize;
+    return min(nb, p.max_blocks) * UH;
+}
+
 template <typename T>
 __device__ __forceinline__ T shfl(T v, int src) {
     return __shfl_sync(0xffffffffu, v, src);
@@ -118,15 +130,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     const bool mixed = p.query_start_loc != nullptr;
 
     // ---- prologue: blocks per unit of every sequence, exclusive scan -> cum ----
-    auto eligible = [&](int s) -> bool {
-        return !mixed || (p.query_start_loc[s + 1] - p.query_start_loc[s] == 1);
-    };
-    auto unit_blocks = [&](int s) -> int {
-        if (!eligible(s)) return 0;
-        int n = p.seq_lens[s];
-        int nb = (max(n, 0) + kBlockSize - 1) / kBlockSize;
-        return min(nb, p.max_blocks) * UH;
-    };
+    auto eligible = [&](int s) -> bool { return decode_row(p, s); };
+    auto unit_blocks = [&](int s) -> int { return unit_blocks_of(p, s, UH); };
     {
         const int per = (B + blockDim.x - 1) / blockDim.x;
         const int beg = min(B, static_cast<int>(threadIdx.x) * per);
@@ -163,10 +168,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     }
     __syncthreads();
     grid_launch_dependents();
-    if (blockIdx.x == 0) {
-        // the block prefix and worker count, for the combine kernel
+    if (B > kCombineScanSeqs && blockIdx.x == 0) {
+        // the block prefix, for the combine kernel of a large batch
         for (int i = threadIdx.x; i <= B; i += blockDim.x) p.plan[i] = cum[i];
-        if (threadIdx.x == 0) p.plan[B + 1] = static_cast<int>(min(static_cast<long long>(p.num_workers), static_cast<long long>(cum[B])));
     }
 
     const long long T = cum[B];
@@ -486,92 +490,99 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
 // Log-sum-exp combine of the units split across workers:
 //   out = sum_i e^{m_i - M} o_i / sum_i e^{m_i - M} l_i,   M = max_i m_i,
 // where worker i left its unnormalised output o_i, running max m_i (log2 units)
-// and running sum l_i.  One CTA per unit, one warp per 16-wide slice of d.
-// Pass 1 reads every slot's (m, l) with lanes in parallel and reduces over the
-// warp; pass 2 reads up to 16 slots' fragments per round trip, the first 16
-// requested together with pass 1.
+// and running sum l_i.  One CTA per unit, one warp per 16-wide slice of d; a
+// lane owns heads 2t, 2t+1 of the fragment layout.  Before waiting for the
+// decode grid, the CTA finds its unit's place in the flattened order from the
+// lengths (the decode grid computes the same prefix); after it, one round trip
+// brings up to 16 slots' fragments together with their (m, l) for the lane's two
+// heads, reduced in registers (online across batches of 16): no shuffles.
 template <bool OutBf16, bool Fp8Layout>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
-    grid_dependency_wait();
     const int UH = p.num_kv_heads * p.head_groups;
     const int u = blockIdx.x;
     const int s = u / UH, uh = u % UH;
     const int B = p.num_seqs;
-    const int lo = p.plan[s], hi = p.plan[s + 1];
-    const int W = p.plan[B + 1];
-    const long long T = p.plan[B];
-    if (hi == lo || W <= 0) return;
-    const int nb = (hi - lo) / UH;
+    const int dt = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
+    long long lo = 0, T = 0;
+    if (B <= kCombineScanSeqs) {
+        // the prefix from the lengths, overlapping the decode grid's tail
+        __shared__ long long red[2][8];
+        long long before = 0, total = 0;
+        for (int i = threadIdx.x; i < B; i += blockDim.x) {
+            const int nbl = unit_blocks_of(p, i, UH);
+            total += nbl;
+            if (i < s) before += nbl;
+        }
+#pragma unroll
+        for (int o2 = 16; o2 >= 1; o2 >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, o2);
+            total += __shfl_xor_sync(0xffffffffu, total, o2);
+        }
+        if (lane == 0) {
+            red[0][dt] = before;
+            red[1][dt] = total;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            lo += red[0][k];
+            T += red[1][k];
+        }
+    } else {
+        grid_dependency_wait();
+        lo = p.plan[s];
+        T = p.plan[B];
+    }
+    const int nb = unit_blocks_of(p, s, UH) / UH;
+    const int W = static_cast<int>(min(static_cast<long long>(p.num_workers), T));
+    if (nb == 0 || W <= 0) return;
     const long long fu = lo + static_cast<long long>(uh) * nb;
     const int wa = worker_of(fu, T, W), wb = worker_of(fu + nb - 1, T, W);
     if (wa == wb) return;   // its only worker wrote the output
     const int nseg = wb - wa + 1;
-    const int dt = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
 
-    // first batch of fragments and every slot's (m, l) are requested together
-    float4 v[16];
-    float m0v[16], m1v[16];
-    auto load_batch = [&](int base) {
+    if (B <= kCombineScanSeqs) grid_dependency_wait();
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int base = 0; base < nseg; base += 16) {
+        float4 v[16];
+        float2 mv[16], lv[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const int sl = wa + min(base + k, nseg - 1) + u;
             v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
-            m0v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t);
-            m1v[k] = __ldcg(p.ml + static_cast<size_t>(sl) * 16 + 2 * t + 1);
+            mv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 2 * t));
+            lv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 8 + 2 * t));
         }
-    };
-    load_batch(0);
-
-    float Mh[8], Lh[8];
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-        Mh[h] = -INFINITY;
-        Lh[h] = 0.f;
-    }
-    for (int base = 0; base < nseg; base += 32) {
-        const bool live = base + lane < nseg;
-        float mv[8], lv[8];
-        if (live) {
-            const float4* ml4 = reinterpret_cast<const float4*>(p.ml + static_cast<size_t>(wa + base + lane + u) * 16);
-            const float4 a = __ldcg(ml4), b = __ldcg(ml4 + 1), c = __ldcg(ml4 + 2), d = __ldcg(ml4 + 3);
-            mv[0] = a.x; mv[1] = a.y; mv[2] = a.z; mv[3] = a.w; mv[4] = b.x; mv[5] = b.y; mv[6] = b.z; mv[7] = b.w;
-            lv[0] = c.x; lv[1] = c.y; lv[2] = c.z; lv[3] = c.w; lv[4] = d.x; lv[5] = d.y; lv[6] = d.z; lv[7] = d.w;
-        } else {
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                mv[h] = -INFINITY;
-                lv[h] = 0.f;
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            float mx = mv[h];
-#pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-            const float nm = fmaxf(Mh[h], mx);
-            float c = live ? lv[h] * exp2f(mv[h] - nm) : 0.f;
-#pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) c += __shfl_xor_sync(0xffffffffu, c, o2);
-            Lh[h] = Lh[h] * exp2f(Mh[h] - nm) + c;
-            Mh[h] = nm;
-        }
-    }
-    const float M0 = t == 0 ? Mh[0] : t == 1 ? Mh[2] : t == 2 ? Mh[4] : Mh[6];
-    const float M1 = t == 0 ? Mh[1] : t == 1 ? Mh[3] : t == 2 ? Mh[5] : Mh[7];
-    const float L0 = t == 0 ? Lh[0] : t == 1 ? Lh[2] : t == 2 ? Lh[4] : Lh[6];
-    const float L1 = t == 0 ? Lh[1] : t == 1 ? Lh[3] : t == 2 ? Lh[5] : Lh[7];
-
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int base = 0; base < nseg; base += 16) {
-        if (base > 0) load_batch(base);
+        const int n = min(16, nseg - base);
+        float b0 = M0, b1 = M1;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-            if (base + k < nseg) {
-                const float w0 = exp2f(m0v[k] - M0), w1 = exp2f(m1v[k] - M1);
+            if (k < n) {
+                b0 = fmaxf(b0, mv[k].x);
+                b1 = fmaxf(b1, mv[k].y);
+            }
+        }
+        // rescale what earlier batches summed (nothing on the first batch)
+        const float r0 = base > 0 ? exp2f(M0 - b0) : 0.f, r1 = base > 0 ? exp2f(M1 - b1) : 0.f;
+        acc[0] *= r0;
+        acc[2] *= r0;
+        acc[1] *= r1;
+        acc[3] *= r1;
+        L0 *= r0;
+        L1 *= r1;
+        M0 = b0;
+        M1 = b1;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k < n) {
+                const float w0 = exp2f(mv[k].x - M0), w1 = exp2f(mv[k].y - M1);
                 acc[0] += v[k].x * w0;
                 acc[1] += v[k].y * w1;
                 acc[2] += v[k].z * w0;
                 acc[3] += v[k].w * w1;
+                L0 += lv[k].x * w0;
+                L1 += lv[k].y * w1;
             }
         }
     }

@@ -281,7 +281,7 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_kv_heads, int head
     const size_t slots = units + static_cast<size_t>(workers);
     l.status_off = 0;
     l.plan_off = 256;
-    l.ml_off = l.plan_off + round_up((static_cast<size_t>(num_seqs) + 2) * 4, 256);
+    l.ml_off = l.plan_off + round_up((static_cast<size_t>(num_seqs) + 1) * 4, 256);
     l.partial_off = l.ml_off + round_up(slots * 16 * 4, 256);
     l.total = l.partial_off + slots * 8 * 32 * sizeof(float4);
     return l;

@@ -15,7 +15,11 @@ constexpr int kBlockSize = 16;
 constexpr int kMaxSeqs = 8192;
 constexpr int kDecodeWarps = 4;        // warps per decode CTA
 constexpr int kMaxDecodeCtasPerSm = 2;
-constexpr int kHeadsPerGroup = 8;      // query heads handled by one decode unit (MMA N)
+constexpr int kHeadsPerGroup = 8;
+// Up to this many sequences the combine kernel finds a unit's place in the flattened
+// order itself (before waiting for the decode grid); above it the decode grid
+// publishes its block prefix in the workspace.
+constexpr int kCombineScanSeqs = 1024;      // query heads handled by one decode unit (MMA N)
 
 // Bits of the device-side status word (first word of the workspace).
 constexpr int kDevErrTimeout = 1;
@@ -35,7 +39,7 @@ struct DecodeParams {
     const float* k_scale;
     const float* v_scale;
     int* status;                      // device status word
-    int* plan;                        // [num_seqs + 2]: block prefix per sequence, then workers used
+    int* plan;                        // [num_seqs + 1]: block prefix per sequence (large batches only)
     float* ml;                        // [slots][16]: running max (8 heads), sum (8 heads)
     float4* partial;                  // [slots][8][32]: unnormalised output fragments
     int num_seqs;
