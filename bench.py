@@ -184,7 +184,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_step(w: W.Workload, pa, ws, outs, layers_caches, decode_only_kernels=False):
+def build_step(w: W.Workload, pa, ws, outs, layers_caches, decode_only_kernels=False, cascade=False):
     """Enqueue one step on the current stream (used inside graph capture)."""
     for layer in range(w.num_layers):
         kc, vc = layers_caches[layer]
@@ -192,7 +192,10 @@ def build_step(w: W.Workload, pa, ws, outs, layers_caches, decode_only_kernels=F
         vs = w.v_scale[layer:layer + 1] if w.v_scale is not None else None
         if w.num_new_tokens and not decode_only_kernels:
             pa.pa_reshape_and_cache(w.k_new[layer], w.v_new[layer], kc, vc, w.slot_mapping, ks, vs)
-        if w.is_decode_only:
+        if w.is_decode_only and cascade:
+            pa.pa_decode_shared_prefix(outs[layer], w.q[layer], kc, vc, w.block_tables, w.seq_lens,
+                                       w.shared_prefix_blocks, w.scale, ws, ks, vs)
+        elif w.is_decode_only:
             pa.pa_decode(outs[layer], w.q[layer], kc, vc, w.block_tables, w.seq_lens, w.scale, ws, ks, vs)
         else:
             pa.pa_mixed(outs[layer], w.q[layer], w.query_start_loc, kc, vc, w.block_tables, w.seq_lens,
@@ -222,10 +225,15 @@ def run_ours(args, rank, world, local):
     ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, device=dev)
     outs = [torch.empty_like(w.q[l]) for l in range(w.num_layers)]
     kv_bytes = kv_read_bytes(w)
-    step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches))
-    decode_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, decode_only_kernels=True))
+    cascade = bool(args.cascade)
+    if cascade and not (w.is_decode_only and w.shared_prefix_blocks > 0):
+        raise SystemExit("--cascade needs a decode workload whose tables share leading blocks (shared-prefix)")
+    step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, cascade=cascade))
+    decode_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, decode_only_kernels=True,
+                                              cascade=cascade))
     # per layer: the slot write, the attention kernel and its combine, the chunk kernel of a mixed batch
-    launches_per_step = w.num_layers * ((1 if w.num_new_tokens else 0) + 2 + (0 if w.is_decode_only else 1))
+    launches_per_step = w.num_layers * ((1 if w.num_new_tokens else 0) + 2 +
+                                        (0 if w.is_decode_only and not cascade else 1))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     unique_bytes = sum(c.numel() * c.element_size() * 2 for c in w.k_cache)
     flush = unique_bytes < 2 * l2
@@ -303,8 +311,13 @@ def run_ours(args, rank, world, local):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     value = kv_bytes * world / (ms * 1e-3) / 1e9
     per_launch_bytes = kv_bytes / w.num_layers
+    if cascade:
+        # the cascade reads the shared blocks once: its roofline counts unique bytes
+        tok = sum(int(n) - w.shared_prefix_blocks * W.BLOCK_SIZE for n in w.seq_lens.tolist())
+        tok += w.shared_prefix_blocks * W.BLOCK_SIZE
+        per_launch_bytes = tok * 2 * w.num_kv_heads * w.head_dim * ELEM[w.cache_dtype]
     achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = None if cascade else recorded_traffic(args.workload)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -324,7 +337,8 @@ def run_ours(args, rank, world, local):
             "kv_bytes_per_step": kv_bytes,
             "launch": f"one CUDA graph per step: {w.num_layers} x ("
                       + ("pa_reshape_and_cache + " if w.num_new_tokens else "")
-                      + ("pa_decode" if w.is_decode_only else "pa_mixed") + ")",
+                      + (("pa_decode_shared_prefix" if cascade else "pa_decode") if w.is_decode_only
+                         else "pa_mixed") + ")",
             "l2": ("L2 flushed between steps" if flush else
                    f"inputs larger than L2 ({unique_bytes / 1e9:.2f} GB of cache vs {l2 / 1e6:.0f} MB L2)"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -333,7 +347,7 @@ def run_ours(args, rank, world, local):
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / hbm_peak, 2),
         "roofline": {
-            "kernel": "pa_decode",
+            "kernel": "pa_decode_shared_prefix (unique bytes: prefix once + suffixes)" if cascade else "pa_decode",
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": hbm_peak,
@@ -382,7 +396,7 @@ def run_e2e(args, w, pa, ws, outs, layers_caches, dev):
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     h2d = sum(t.numel() * t.element_size() for t in pinned)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    g = capture(lambda: build_step(w, pa, ws, outs, layers_caches))
+    g = capture(lambda: build_step(w, pa, ws, outs, layers_caches, cascade=bool(args.cascade)))
     stream = torch.cuda.current_stream()
 
     def step():
@@ -485,6 +499,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.NAMED))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix workload through pa_decode_shared_prefix (prefix once on the tensor cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)

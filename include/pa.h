@@ -168,6 +168,40 @@ PA_API pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, con
                        int num_workers, pa_stream_t stream);
 
 /*
+ * Decode for a batch whose block tables share their leading blocks: the same
+ * result as pa_decode, computed in cascade.  The pages describe requests that
+ * start with the same prompt reusing the same full KV blocks, so that their
+ * block tables point at the same physical blocks [P3 "Prefix caching is the
+ * second win"; P1 s.4 block table, s.5 prefix caching]; they give no kernel for
+ * it (the cascade split below is this library's).
+ *
+ * Precondition: for every sequence s, block_tables[s][j] == block_tables[0][j]
+ * for j < prefix_blocks, and seq_lens[s] >= 16 * prefix_blocks.  A batch that
+ * violates it is recorded as PA_ERR_OUT_OF_RANGE in the workspace status word
+ * (its outputs are then unspecified).
+ *
+ * The prefix keys are read once for the whole batch: every decode row of every
+ * sequence is contracted against them on the tensor cores as one dense tile
+ * grid (one CTA per 256 query rows of a KV head), leaving an unnormalised
+ * partial per row; the private blocks after the prefix stream through the
+ * decode kernel, launched behind it and running beside it; the combine kernel
+ * merges both by log-sum-exp.  prefix_blocks == 0 reduces to pa_decode with
+ * every row merged by the combine.
+ *
+ *   prefix_blocks  host, 0 <= prefix_blocks <= max_blocks_per_seq
+ *   workspace      at least pa_workspace_size(num_seqs, num_q_heads,
+ *                  num_kv_heads, head_dim) bytes
+ * Other arguments as pa_decode; results agree with pa_decode to rounding.
+ */
+PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* seq_lens, int num_seqs, int prefix_blocks,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                                  const float* k_scale, const float* v_scale, void* workspace,
+                                  size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * Mixed batch: decode rows and prefill chunks in one flattened query array
  * [P3 "Batching does not merge the conversations"; P1 s.6 chunked prefill].
  *

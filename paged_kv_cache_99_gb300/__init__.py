@@ -65,6 +65,8 @@ def _lib():
     lib.pa_decode.restype = I
     lib.pa_decode_ex.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, I, P]
     lib.pa_decode_ex.restype = I
+    lib.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
+    lib.pa_decode_shared_prefix.restype = I
     lib.pa_mixed.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
     lib.pa_mixed.restype = I
     lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P]
@@ -160,6 +162,29 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, workspace
                              _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale), _ptr(v_scale),
                              _ptr(workspace), workspace.numel(), int(num_workers), _stream(stream))
     _check(st, "pa_decode")
+
+
+def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, prefix_blocks, scale, workspace,
+                            k_scale=None, v_scale=None, stream=None):
+    """pa_decode for tables that share their first prefix_blocks entries (cascade: the shared
+    prefix as one dense tensor-core contraction, the private suffixes through the decode kernel)."""
+    _need(q, "q", (torch.bfloat16, torch.float16))
+    _need(out, "out", (q.dtype,))
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, tuple(_DTYPE))
+    _need(block_tables, "block_tables", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(workspace, "workspace", (torch.uint8,))
+    B, Hq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    if out.shape != q.shape or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    st = _lib().pa_decode_shared_prefix(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        block_tables.shape[1], _ptr(seq_lens), B, int(prefix_blocks), Hq, Hkv, d,
+                                        bs, nb, float(scale), _DTYPE[q.dtype], _DTYPE[k_cache.dtype],
+                                        _ptr(k_scale), _ptr(v_scale), _ptr(workspace), workspace.numel(),
+                                        _stream(stream))
+    _check(st, "pa_decode_shared_prefix")
 
 
 def pa_mixed(out, q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, max_q_len, scale, workspace,

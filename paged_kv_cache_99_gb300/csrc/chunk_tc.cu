@@ -153,69 +153,87 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
 
     grid_dependency_wait();
 
-    // ---- tile pairs per chunk sequence, exclusive scan -> cum ----
     const int B = p.num_seqs;
     const int QT = p.queries_per_tile;
-    auto pairs_of = [&](int s) -> int {
-        const int ql = p.query_start_loc[s + 1] - p.query_start_loc[s];
-        return ql >= 2 ? (ql + 2 * QT - 1) / (2 * QT) : 0;
-    };
-    {
-        const int per = (B + kThreads - 1) / kThreads;
-        const int beg = min(B, static_cast<int>(threadIdx.x) * per);
-        const int end = min(B, beg + per);
-        int local = 0;
-        for (int s = beg; s < end; ++s) local += pairs_of(s);
-        int incl = local;
+    const bool prefix = p.prefix_keys > 0;
+    int s = 0, pair = 0, q0 = 0, q_len = 0, n = 0;
+    if (!prefix) {
+        // ---- tile pairs per chunk sequence, exclusive scan -> cum ----
+        auto pairs_of = [&](int sq) -> int {
+            const int ql = p.query_start_loc[sq + 1] - p.query_start_loc[sq];
+            return ql >= 2 ? (ql + 2 * QT - 1) / (2 * QT) : 0;
+        };
+        {
+            const int per = (B + kThreads - 1) / kThreads;
+            const int beg = min(B, static_cast<int>(threadIdx.x) * per);
+            const int end = min(B, beg + per);
+            int local = 0;
+            for (int sq = beg; sq < end; ++sq) local += pairs_of(sq);
+            int incl = local;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) warp_tot[warp] = incl;
+            __syncthreads();
+            int run = incl - local;
+            for (int w = 0; w < warp; ++w) run += warp_tot[w];
+            for (int sq = beg; sq < end; ++sq) {
+                cum[sq] = run;
+                run += pairs_of(sq);
+            }
+            if (threadIdx.x == kThreads - 1) cum[B] = run;
         }
-        if (lane == 31) warp_tot[warp] = incl;
         __syncthreads();
-        int run = incl - local;
-        for (int w = 0; w < warp; ++w) run += warp_tot[w];
-        for (int s = beg; s < end; ++s) {
-            cum[s] = run;
-            run += pairs_of(s);
-        }
-        if (threadIdx.x == kThreads - 1) cum[B] = run;
-    }
-    __syncthreads();
-    grid_launch_dependents();
+        grid_launch_dependents();
 
-    const int R = cum[B];
-    if (static_cast<int>(blockIdx.x) >= R) return;
-    const int tau = R - 1 - static_cast<int>(blockIdx.x);   // heaviest pairs first
-    int s = 0;
-    {
-        int lo = 0, hi = B;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cum[mid] <= tau) lo = mid; else hi = mid;
+        const int R = cum[B];
+        if (static_cast<int>(blockIdx.x) >= R) return;
+        const int tau = R - 1 - static_cast<int>(blockIdx.x);   // heaviest pairs first
+        {
+            int lo = 0, hi = B;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (cum[mid] <= tau) lo = mid; else hi = mid;
+            }
+            s = lo;
         }
-        s = lo;
+        pair = tau - cum[s];
+        q0 = p.query_start_loc[s];
+        q_len = p.query_start_loc[s + 1] - q0;
+        n = p.seq_lens[s];
+        if (n - q_len < 0 || n > p.max_blocks * kBlockSize) {   // inconsistent lengths
+            if (threadIdx.x == 0) atomicOr(p.status, kDevErrRange);
+            return;
+        }
+    } else {
+        // ---- prefix mode: query j is the decode row of sequence j; keys are the
+        // shared prefix, read through sequence 0's table ----
+        grid_launch_dependents();
+        pair = blockIdx.x;
+        q_len = B;
+        n = p.prefix_keys;
+        if (2 * pair * QT >= B) return;
+        if (n > p.max_blocks * kBlockSize) {
+            if (threadIdx.x == 0) atomicOr(p.status, kDevErrRange);
+            return;
+        }
     }
-    const int pair = tau - cum[s];
     const int h = blockIdx.y;
     const int G = p.group;
-    const int q0 = p.query_start_loc[s];
-    const int q_len = p.query_start_loc[s + 1] - q0;
-    const int n = p.seq_lens[s];
-    if (n - q_len < 0 || n > p.max_blocks * kBlockSize) {   // inconsistent lengths
-        if (threadIdx.x == 0) atomicOr(p.status, kDevErrRange);
-        return;
-    }
+    // position of query j: causal chunk rows follow the cached tokens; in prefix mode
+    // every row sits after the whole prefix
+    auto qpos = [&](int j) -> int { return prefix ? n - 1 : n - q_len + j; };
     // tile X (0 = A, 1 = B): queries j_first[X] .. j_last[X]; B may be absent
     const int jf0 = 2 * pair * QT;
     const int jf1 = jf0 + QT;
     const bool has_b = jf1 < q_len;
     const int jl0 = min(q_len, jf0 + QT) - 1;
     const int jl1 = has_b ? min(q_len, jf1 + QT) - 1 : jl0;
-    const int pos_last_cta = n - q_len + jl1;
+    const int pos_last_cta = qpos(jl1);
     const int nsteps = pos_last_cta / kTcKeys + 1;
-    const int nsteps_a = (n - q_len + jl0) / kTcKeys + 1;
+    const int nsteps_a = qpos(jl0) / kTcKeys + 1;
     const int nblocks = pos_last_cta / kBlockSize + 1;
     const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
     auto tile_steps = [&](int x) -> int { return x == 0 ? nsteps_a : (has_b ? nsteps : 0); };
@@ -364,8 +382,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         const int jl = x == 0 ? jl0 : jl1;
         const int jq = r / G;
         const bool live = steps > 0 && r < QT * G && jf + jq <= jl;
-        const int pos_first = n - q_len + jf;
-        const int pos = live ? n - q_len + jf + jq : n - q_len + jl;
+        const int pos_first = qpos(jf);
+        const int pos = live ? qpos(jf + jq) : qpos(jl);
         const size_t qrow = (static_cast<size_t>(q0 + (live ? jf + jq : jf0)) * p.num_q_heads + h * G +
                              (live ? r % G : 0)) * kHeadDim;
         // Q row -> shared memory (MMA input type), 128-byte swizzle, two d-halves
@@ -502,7 +520,27 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         }
         // ---- epilogue: O / l ----
         if (steps > 0) {
-            if (ok && warp_wait(bar(kBarPvDone + x), 0, p.timeout_ns)) {
+            if (ok && prefix && warp_wait(bar(kBarPvDone + x), 0, p.timeout_ns)) {
+                // unnormalised rows and (max, sum) for the combine of the cascade decode
+                tc_fence_after();
+                float4* dst = reinterpret_cast<float4*>(p.prefix_o + qrow);
+#pragma unroll 1
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO(x) + lane_off + 32 * c, ov);
+                    tmem_wait_ld();
+                    if (live) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[8 * c + e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                                         __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+                    }
+                }
+                if (live) {
+                    p.prefix_ml[(qrow / kHeadDim) * 2] = m_used;
+                    p.prefix_ml[(qrow / kHeadDim) * 2 + 1] = l;
+                }
+            } else if (ok && !prefix && warp_wait(bar(kBarPvDone + x), 0, p.timeout_ns)) {
                 tc_fence_after();
                 const float inv = vscale / l;
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow);

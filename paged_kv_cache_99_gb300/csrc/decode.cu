@@ -78,11 +78,12 @@ __device__ __forceinline__ bool decode_row(const DecodeParams& p, int s) {
     return p.query_start_loc == nullptr || p.query_start_loc[s + 1] - p.query_start_loc[s] == 1;
 }
 
-// Blocks sequence s contributes to the flattened order (its blocks x units).
+// Blocks sequence s contributes to the flattened order (its blocks x units); a
+// cascade decode covers only the blocks after the shared prefix.
 __device__ __forceinline__ int unit_blocks_of(const DecodeParams& p, int s, int UH) {
     if (!decode_row(p, s)) return 0;
     const int nb = (max(p.seq_lens[s], 0) + kBlockSize - 1) / kBlockSize;
-    return min(nb, p.max_blocks) * UH;
+    return max(min(nb, p.max_blocks) - p.first_block, 0) * UH;
 }
 
 template <typename T>
@@ -154,6 +155,18 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         }
         if (threadIdx.x == blockDim.x - 1) cum[B] = run;
     }
+    if (p.cascade) {
+        // every table must start with sequence 0's first_block entries and every
+        // sequence must hold the whole prefix
+        const long long checks = static_cast<long long>(B) * p.first_block;
+        for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < checks;
+             i += static_cast<long long>(gridDim.x) * blockDim.x) {
+            const int s = static_cast<int>(i / p.first_block), j = static_cast<int>(i % p.first_block);
+            if (__ldg(p.block_tables + static_cast<size_t>(s) * p.max_blocks + j) != __ldg(p.block_tables + j) ||
+                (j == 0 && p.seq_lens[s] < p.first_block * kBlockSize))
+                atomicOr(p.status, kDevErrRange);
+        }
+    }
     // empty decode rows produce zeros; over-long sequences are an input error
     for (int s = blockIdx.x; s < B; s += gridDim.x) {
         if (!eligible(s)) continue;
@@ -210,13 +223,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     // ---- producer: block-table window + TMA issue ----
     int tbl_s = -1, tbl_j0 = -1, tbl = 0;
     auto issue = [&](const Cursor& c, int k) {
-        if (c.s != tbl_s || (c.j & ~31) != tbl_j0) {
+        const int ja = c.j + p.first_block;      // table index of the cursor's block
+        if (c.s != tbl_s || (ja & ~31) != tbl_j0) {
             tbl_s = c.s;
-            tbl_j0 = c.j & ~31;
+            tbl_j0 = ja & ~31;
             const int jj = tbl_j0 + lane;
-            tbl = jj < c.nb ? __ldg(p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + jj) : 0;
+            tbl = jj < c.nb + p.first_block ? __ldg(p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + jj) : 0;
         }
-        int phys = shfl(tbl, c.j & 31);
+        int phys = shfl(tbl, ja & 31);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
             if (lane == 0) atomicOr(p.status, kDevErrRange);
             phys = 0;
@@ -310,7 +324,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
 
         const uint32_t kt = my_tiles + st * STAGE;
         const uint32_t vt = kt + TILE;
-        const int valid = min(kBlockSize, n_cur - C.j * kBlockSize);
+        const int valid = min(kBlockSize, n_cur - (C.j + p.first_block) * kBlockSize);
 
         // ---- S^T = K . Q^T : rows = 16 keys, cols = 8 heads ----
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -429,7 +443,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
             }
             const int u = C.s * UH + C.uh;
             const long long fu = cum[C.s] + static_cast<long long>(C.uh) * C.nb;
-            const bool write = worker_of(fu, T, W) == worker_of(fu + C.nb - 1, T, W);
+            // a unit one worker covers is written directly, unless a prefix partial waits for it
+            const bool write = !p.cascade && worker_of(fu, T, W) == worker_of(fu + C.nb - 1, T, W);
             if (!write) {
                 // unit shared with other workers: plain partial store, merged by combine_kernel
                 const int slot = wid + u;
@@ -487,6 +502,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
     if (p.overlap_prior && blockIdx.x == gridDim.x - 1) grid_dependency_wait();
 }
 
+constexpr int kBatch = 8;   // slots per round trip of the combine
+
 // Log-sum-exp combine of the units split across workers:
 //   out = sum_i e^{m_i - M} o_i / sum_i e^{m_i - M} l_i,   M = max_i m_i,
 // where worker i left its unnormalised output o_i, running max m_i (log2 units)
@@ -494,12 +511,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
 // lane owns heads 2t, 2t+1 of the fragment layout.  Before waiting for the
 // decode grid, the CTA finds its unit's place in the flattened order from the
 // lengths (the decode grid computes the same prefix); after it, one round trip
-// brings up to 16 slots' fragments together with their (m, l) for the lane's two
-// heads, reduced in registers (online across batches of 16): no shuffles.
+// brings up to kBatch slots' fragments together with their (m, l) for the lane's
+// two heads, reduced in registers (online across batches): no shuffles.
 template <bool OutBf16, bool Fp8Layout>
-__global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
+__device__ __forceinline__ void combine_unit(const DecodeParams& p, int u) {
     const int UH = p.num_kv_heads * p.head_groups;
-    const int u = blockIdx.x;
     const int s = u / UH, uh = u % UH;
     const int B = p.num_seqs;
     const int dt = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
@@ -507,6 +523,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
     if (B <= kCombineScanSeqs) {
         // the prefix from the lengths, overlapping the decode grid's tail
         __shared__ long long red[2][8];
+        __syncthreads();          // the previous unit's readers of red are done
         long long before = 0, total = 0;
         for (int i = threadIdx.x; i < B; i += blockDim.x) {
             const int nbl = unit_blocks_of(p, i, UH);
@@ -535,36 +552,61 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
     }
     const int nb = unit_blocks_of(p, s, UH) / UH;
     const int W = static_cast<int>(min(static_cast<long long>(p.num_workers), T));
-    if (nb == 0 || W <= 0) return;
-    const long long fu = lo + static_cast<long long>(uh) * nb;
-    const int wa = worker_of(fu, T, W), wb = worker_of(fu + nb - 1, T, W);
-    if (wa == wb) return;   // its only worker wrote the output
-    const int nseg = wb - wa + 1;
+    const bool pre = p.cascade && p.first_block > 0;   // every row has a shared-prefix partial
+    int wa = 0, nseg = 0;
+    if (nb > 0 && W > 0) {
+        const long long fu = lo + static_cast<long long>(uh) * nb;
+        wa = worker_of(fu, T, W);
+        const int wb = worker_of(fu + nb - 1, T, W);
+        if (wa == wb && !p.cascade) return;   // its only worker wrote the output
+        nseg = wb - wa + 1;
+    } else if (!pre) {
+        return;   // an empty row: the decode grid wrote its zeros
+    }
+    const int h = uh / p.head_groups;
+    const int hg = uh % p.head_groups;
+    const int row = p.query_start_loc ? p.query_start_loc[s] : s;
 
     if (B <= kCombineScanSeqs) grid_dependency_wait();
     float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int base = 0; base < nseg; base += 16) {
-        float4 v[16];
-        float2 mv[16], lv[16];
+    if (pre) {
+        // start from the shared-prefix partial of the lane's two heads, in the
+        // fragment layout of the decode partials
+        const int dA = Fp8Layout ? 16 * dt + 2 * g : 16 * dt + g;
+        const int dB = Fp8Layout ? dA + 1 : dA + 8;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int e = 0; e < 2; ++e) {
+            const int gh = hg * kHeadsPerGroup + 2 * t + e;
+            if (gh >= p.group) continue;
+            const size_t ri = static_cast<size_t>(row) * p.num_q_heads + h * p.group + gh;
+            const float m = __ldcg(p.prefix_ml + 2 * ri), lsum = __ldcg(p.prefix_ml + 2 * ri + 1);
+            if (e == 0) { M0 = m; L0 = lsum; } else { M1 = m; L1 = lsum; }
+            acc[e] = __ldcg(p.prefix_o + ri * kHeadDim + dA);
+            acc[2 + e] = __ldcg(p.prefix_o + ri * kHeadDim + dB);
+        }
+    }
+    for (int base = 0; base < nseg; base += kBatch) {
+        float4 v[kBatch];
+        float2 mv[kBatch], lv[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
             const int sl = wa + min(base + k, nseg - 1) + u;
             v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
             mv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 2 * t));
             lv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 8 + 2 * t));
         }
-        const int n = min(16, nseg - base);
+        const int n = min(kBatch, nseg - base);
         float b0 = M0, b1 = M1;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < kBatch; ++k) {
             if (k < n) {
                 b0 = fmaxf(b0, mv[k].x);
                 b1 = fmaxf(b1, mv[k].y);
             }
         }
-        // rescale what earlier batches summed (nothing on the first batch)
-        const float r0 = base > 0 ? exp2f(M0 - b0) : 0.f, r1 = base > 0 ? exp2f(M1 - b1) : 0.f;
+        // rescale what is summed so far (zero while nothing is: M = -inf)
+        const float r0 = exp2f(M0 - b0), r1 = exp2f(M1 - b1);
         acc[0] *= r0;
         acc[2] *= r0;
         acc[1] *= r1;
@@ -574,7 +616,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
         M0 = b0;
         M1 = b1;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < kBatch; ++k) {
             if (k < n) {
                 const float w0 = exp2f(mv[k].x - M0), w1 = exp2f(mv[k].y - M1);
                 acc[0] += v[k].x * w0;
@@ -587,9 +629,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
         }
     }
     const float vscale = Fp8Layout ? __ldg(p.v_scale) : 1.0f;
-    const int h = uh / p.head_groups;
-    const int hg = uh % p.head_groups;
-    const int row = p.query_start_loc ? p.query_start_loc[s] : s;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int gh = hg * kHeadsPerGroup + 2 * t + e;
@@ -607,6 +646,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
             orow[16 * dt + g + 8] = hi16;
         }
     }
+}
+
+// Grid-stride over the units: a few CTAs per SM (about 100 registers per thread
+// with 8-slot batches) cover any number of units without waves of one-CTA SMs.
+template <bool OutBf16, bool Fp8Layout>
+__global__ void __launch_bounds__(256, 2) combine_kernel(const DecodeParams p) {
+    const long long units = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.head_groups;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) combine_unit<OutBf16, Fp8Layout>(p, static_cast<int>(u));
 }
 
 // ---------------------------------------------------------------------------
@@ -683,10 +730,11 @@ cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, 
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, int max_ctas,
+                           cudaStream_t stream) {
     const long long units = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.head_groups;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(units));
+    cfg.gridDim = dim3(static_cast<unsigned>(units < max_ctas ? units : max_ctas));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -152,7 +152,8 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
                       const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads, float scale,
                       pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
                       void* workspace, size_t workspace_bytes, int num_workers, int num_blocks,
-                      cudaStream_t stream, bool overlap_prior = false) {
+                      cudaStream_t stream, bool overlap_prior = false, bool cascade = false,
+                      int first_block = 0) {
     int dev = 0;
     DeviceState* st = device_state(&dev);
     if (!st) return PA_ERR_CUDA;
@@ -184,7 +185,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     if (num_workers < 0 || num_workers > max_workers(*st)) return PA_ERR_INVALID_ARG;
     const int W = num_workers == 0 ? full : num_workers;
     const int hg = head_groups_of(num_q_heads, num_kv_heads);
-    const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_kv_heads, hg, W);
+    const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, hg, W);
     if (workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
 
     CUtensorMap kmap, vmap;
@@ -215,12 +216,16 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.num_blocks = num_blocks;
     p.num_workers = W;
     p.overlap_prior = overlap_prior ? 1 : 0;
+    p.cascade = cascade ? 1 : 0;
+    p.first_block = cascade ? first_block : 0;
+    p.prefix_o = reinterpret_cast<const float*>(ws + lay.prefix_o_off);
+    p.prefix_ml = reinterpret_cast<const float*>(ws + lay.prefix_ml_off);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
     s = cuda_status(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream), "launch(decode)");
     if (s != PA_OK) return s;
-    return cuda_status(launch_combine(q_bf16, kind == kKindFp8, p, stream), "launch(combine)");
+    return cuda_status(launch_combine(q_bf16, kind == kKindFp8, p, 2 * st->sms, stream), "launch(combine)");
 }
 
 pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
@@ -228,7 +233,8 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
                      const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* seq_lens, int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
                      int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
-                     const float* v_scale, void* workspace, cudaStream_t stream) {
+                     const float* v_scale, void* workspace, cudaStream_t stream, int prefix_blocks = 0,
+                     float* prefix_o = nullptr, float* prefix_ml = nullptr) {
     DeviceState* st = device_state(nullptr);
     if (!st) return PA_ERR_CUDA;
     const CacheKind kind = kind_of(cache_dtype);
@@ -247,7 +253,9 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
         }
     }
     const int per_cta = qt * chunk_tiles_per_cta();   // queries of one chunk per CTA
-    const long long grid_x = static_cast<long long>(num_seqs) + (total_q + per_cta - 1) / per_cta;
+    // prefix mode: the queries are the sequences' decode rows, one tile pair per CTA
+    const long long grid_x = prefix_blocks > 0 ? (num_seqs + per_cta - 1) / per_cta
+                                               : static_cast<long long>(num_seqs) + (total_q + per_cta - 1) / per_cta;
     if (grid_x >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     ChunkParams p;
     p.out = out;
@@ -267,6 +275,9 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = num_blocks;
     p.queries_per_tile = qt;
+    p.prefix_keys = prefix_blocks * kBlockSize;
+    p.prefix_o = prefix_o;
+    p.prefix_ml = prefix_ml;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     return cuda_status(launch_chunk(kind, q_bf16, kmap, vmap, p, static_cast<int>(grid_x), smem, stream),
@@ -275,13 +286,19 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
 
 }  // namespace
 
-WorkspaceLayout decode_workspace_layout(int num_seqs, int num_kv_heads, int head_groups, int workers) {
+WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_groups,
+                                        int workers) {
     WorkspaceLayout l;
     const size_t units = static_cast<size_t>(num_seqs) * num_kv_heads * head_groups;
     const size_t slots = units + static_cast<size_t>(workers);
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
     l.status_off = 0;
     l.plan_off = 256;
-    l.ml_off = l.plan_off + round_up((static_cast<size_t>(num_seqs) + 1) * 4, 256);
+    // the shared-prefix partials sit before the worker slots: their place does not
+    // depend on the worker count
+    l.prefix_o_off = l.plan_off + round_up((static_cast<size_t>(num_seqs) + 1) * 4, 256);
+    l.prefix_ml_off = l.prefix_o_off + round_up(rows * kHeadDim * sizeof(float), 256);
+    l.ml_off = l.prefix_ml_off + round_up(rows * 2 * sizeof(float), 256);
     l.partial_off = l.ml_off + round_up(slots * 16 * 4, 256);
     l.total = l.partial_off + slots * 8 * 32 * sizeof(float4);
     return l;
@@ -372,7 +389,7 @@ size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int he
         return 0;
     DeviceState* st = device_state(nullptr);
     if (!st) return 0;
-    return decode_workspace_layout(num_seqs, num_kv_heads, head_groups_of(num_q_heads, num_kv_heads),
+    return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_groups_of(num_q_heads, num_kv_heads),
                                    max_workers(*st))
         .total;
 }
@@ -396,6 +413,53 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
                        workspace_bytes, num_workers, num_blocks, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                  int num_seqs, int prefix_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int num_blocks, float scale, pa_dtype q_dtype,
+                                  pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                                  void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+    pa_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                       scale, q_dtype, cache_dtype, k_scale, v_scale, workspace);
+    if (s != PA_OK) return s;
+    if (prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (workspace_bytes < pa_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)) return PA_ERR_WORKSPACE;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (prefix_blocks > 0) {
+        // the shared prefix once, as a dense contraction of every decode row against its keys
+        const CacheKind kind = kind_of(cache_dtype);
+        CUtensorMap kmap, vmap;
+        s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        if (s != PA_OK) return s;
+        s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        if (s != PA_OK) return s;
+        const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads,
+                                                            head_groups_of(num_q_heads, num_kv_heads), 0);
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        s = chunk_impl(out, q, nullptr, k_cache, v_cache, kmap, vmap, block_tables, max_blocks_per_seq, seq_lens,
+                       num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, q_dtype, cache_dtype,
+                       k_scale, v_scale, workspace, cs, prefix_blocks,
+                       reinterpret_cast<float*>(ws + lay.prefix_o_off), reinterpret_cast<float*>(ws + lay.prefix_ml_off));
+        if (s != PA_OK) return s;
+    }
+    // the private suffixes stream beside it, on the SMs the prefix grid leaves free;
+    // the combine merges both
+    int workers = 0;
+    if (prefix_blocks > 0) {
+        DeviceState* st = device_state(nullptr);
+        if (!st) return PA_ERR_CUDA;
+        const int per_cta = (chunk_rows() / (num_q_heads / num_kv_heads)) * chunk_tiles_per_cta();
+        const long long prefix_ctas = static_cast<long long>((num_seqs + per_cta - 1) / per_cta) * num_kv_heads;
+        if (prefix_ctas < st->sms / 2)
+            workers = static_cast<int>(static_cast<long long>(max_workers(*st)) * (st->sms - prefix_ctas) / st->sms);
+    }
+    return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                       num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
+                       workspace_bytes, workers, num_blocks, cs, prefix_blocks > 0, true, prefix_blocks);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -457,8 +521,8 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
     if (s != PA_OK) return s;
     if (num_seqs == 0) return PA_OK;
     // the largest worker count this device can use bounds the scratch a call needs
-    const size_t need = decode_workspace_layout(num_seqs, num_kv_heads, head_groups_of(num_q_heads, num_kv_heads),
-                                                max_workers(*st)).total;
+    const size_t need = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads,
+                                                head_groups_of(num_q_heads, num_kv_heads), max_workers(*st)).total;
     if (need > kNoAllocScratchBytes) {
         snprintf(g_last_error, sizeof g_last_error,
                  "pa_decode_noalloc: this batch needs %zu bytes of scratch; the static scratch holds %zu",

@@ -53,6 +53,13 @@ struct DecodeParams {
     int overlap_prior;                // nonzero: the previous launch is this call's chunk kernel,
                                       // which started only after its own predecessors finished;
                                       // run beside it and wait for it only before exiting
+    // Shared-prefix (cascade) decode: every table starts with the same first_block
+    // physical blocks; the decode grid covers blocks first_block.. only and always
+    // leaves partials, and the combine folds in the prefix partial of each row.
+    int cascade;                      // nonzero: cascade mode
+    int first_block;                  // shared leading blocks (cascade mode)
+    const float* prefix_o;            // [num_seqs][num_q_heads][128]: unnormalised prefix output
+    const float* prefix_ml;           // [num_seqs][num_q_heads][2]: its (max in log2 units, sum)
     float scale_log2;                 // softmax scale * log2(e)
     unsigned long long timeout_ns;    // bound of every barrier wait
 };
@@ -76,6 +83,13 @@ struct ChunkParams {
     int max_blocks;
     int num_blocks;
     int queries_per_tile;             // queries of one sequence per CTA tile
+    // Prefix mode (prefix_keys > 0): the queries are the decode rows of all
+    // sequences ([num_seqs][num_q_heads][128]), every one at position prefix_keys - 1,
+    // the keys are the first prefix_keys tokens of sequence 0's table, and the
+    // output is unnormalised: prefix_o (f32 rows) and prefix_ml (max, sum).
+    int prefix_keys;
+    float* prefix_o;
+    float* prefix_ml;
     float scale_log2;
     unsigned long long timeout_ns;
 };
@@ -85,10 +99,13 @@ struct WorkspaceLayout {
     size_t plan_off;
     size_t ml_off;
     size_t partial_off;
+    size_t prefix_o_off;              // shared-prefix partials: [num_seqs][num_q_heads][128] f32
+    size_t prefix_ml_off;             // and [num_seqs][num_q_heads][2] f32
     size_t total;
 };
 
-WorkspaceLayout decode_workspace_layout(int num_seqs, int num_kv_heads, int head_groups, int slots_workers);
+WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_groups,
+                                        int slots_workers);
 
 // Decode kernels: dynamic shared memory for num_seqs sequences.
 size_t decode_smem_bytes(CacheKind kind, int num_seqs);
@@ -97,7 +114,8 @@ cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas
 cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, const DecodeParams& p, int grid, size_t smem,
                           cudaStream_t stream);
-cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, int max_ctas,
+                           cudaStream_t stream);
 
 // Slot write.
 cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,

@@ -1,0 +1,125 @@
+"""Parity of the shared-prefix (cascade) decode: the shared blocks as one dense
+tensor-core contraction, the private suffixes through the decode kernel, merged
+by the combine.  The result must be the oracle's decode of every row over its
+whole sequence; the precondition (identical leading table entries, sequences at
+least as long as the prefix) is checked on the device."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_99_gb300 as pa
+from paged_kv_cache_99_gb300 import workloads as W
+from tests._gpu import compare, oracle_step
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(seed, prefix, suffixes, G, Hkv=2, cache="bf16", qd="bf16"):
+    lens = [prefix * W.BLOCK_SIZE + x for x in suffixes]
+    return W.build_workload(name="cascade", seed=seed, device=DEV, num_layers=1, seq_lens=lens,
+                            q_lens=[1] * len(lens), num_q_heads=G * Hkv, num_kv_heads=Hkv, q_dtype=qd,
+                            cache_dtype=cache, shared_prefix_blocks=prefix, write_new=False)
+
+
+def _scales(w):
+    return (w.k_scale[0:1] if w.k_scale is not None else None,
+            w.v_scale[0:1] if w.v_scale is not None else None)
+
+
+def _cascade(w, prefix, ws=None, tables=None, lens=None):
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads) if ws is None else ws
+    out = torch.empty_like(w.q[0])
+    ks, vs = _scales(w)
+    pa.pa_decode_shared_prefix(out, w.q[0], w.k_cache[0], w.v_cache[0],
+                               w.block_tables if tables is None else tables,
+                               w.seq_lens if lens is None else lens, prefix, w.scale, ws, ks, vs)
+    torch.cuda.synchronize()
+    return out, pa.pa_read_device_status(ws)
+
+
+# suffix lengths: none, one token, a partial block, exactly one block, one more, longer
+SUFFIXES = [0, 1, 15, 16, 17, 200, 531]
+
+
+@pytest.mark.parametrize("cache,qd", [("bf16", "bf16"), ("fp16", "fp16"), ("fp8", "bf16")])
+@pytest.mark.parametrize("G", [1, 4, 6, 8, 12])
+@pytest.mark.parametrize("prefix", [3, 8])
+def test_cascade_matches_oracle(cache, qd, G, prefix):
+    w = _case(60 + G + prefix, prefix, SUFFIXES, G, cache=cache, qd=qd)
+    out, st = _cascade(w, prefix)
+    assert st == pa.PA_OK, pa.pa_status_string(st)
+    rows, ref = oracle_step(w)
+    compare(out, rows, ref, f"cascade {cache} G={G} prefix={prefix}")
+
+
+@pytest.mark.parametrize("prefix", [37, 40])
+def test_cascade_many_rows_long_prefix(prefix):
+    # 40 sequences x 8 heads: two CTAs per KV head, the second with one tile; 37 blocks
+    # = 592 prefix keys end inside a 128-key step
+    g = np.random.default_rng(prefix)
+    w = _case(70 + prefix, prefix, g.integers(0, 300, 40).tolist(), 8, cache="fp16", qd="fp16")
+    out, st = _cascade(w, prefix)
+    assert st == pa.PA_OK, pa.pa_status_string(st)
+    rows, ref = oracle_step(w)
+    compare(out, rows, ref, f"cascade, prefix {prefix} blocks")
+
+
+def test_cascade_without_prefix_is_decode():
+    w = _case(80, 0, [5, 16, 300, 1, 77], 4)
+    out, st = _cascade(w, 0)
+    assert st == pa.PA_OK
+    rows, ref = oracle_step(w)
+    compare(out, rows, ref, "prefix_blocks = 0")
+
+
+def test_cascade_consecutive_calls_one_workspace():
+    w = _case(81, 5, SUFFIXES, 8, cache="fp8")
+    rows, ref = oracle_step(w)
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads)
+    for prefix in (5, 2, 0, 5):      # any leading part of a shared prefix is itself shared
+        out, st = _cascade(w, prefix, ws=ws)
+        assert st == pa.PA_OK
+        compare(out, rows, ref, f"call with prefix {prefix}")
+
+
+def test_cascade_agrees_with_decode():
+    w = _case(82, 6, SUFFIXES * 3, 6)
+    out, st = _cascade(w, 6)
+    assert st == pa.PA_OK
+    ref_out = torch.empty_like(w.q[0])
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads)
+    pa.pa_decode(ref_out, w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables, w.seq_lens, w.scale, ws)
+    torch.cuda.synchronize()
+    diff = (out.float() - ref_out.float()).abs()
+    assert diff.max().item() <= 1e-2 + 1e-2 * ref_out.float().abs().max().item()
+
+
+def test_cascade_precondition_is_checked():
+    w = _case(83, 4, [10, 20, 30], 4)
+    # a table whose leading entry differs from sequence 0's
+    tables = w.block_tables.clone()
+    tables[1, 2] = tables[2, 4]           # a valid block, but not the shared one
+    _, st = _cascade(w, 4, tables=tables)
+    assert st == pa.PA_ERR_OUT_OF_RANGE
+    # a sequence shorter than the prefix
+    lens = w.seq_lens.clone()
+    lens[2] = 4 * W.BLOCK_SIZE - 3
+    _, st = _cascade(w, 4, lens=lens)
+    assert st == pa.PA_ERR_OUT_OF_RANGE
+    # the same workspace then serves a valid call
+    out, st = _cascade(w, 4)
+    assert st == pa.PA_OK
+    rows, ref = oracle_step(w)
+    compare(out, rows, ref, "after rejected calls")
+
+
+def test_cascade_full_size_shared_prefix_sampled():
+    w = W.make("shared-prefix", DEV)
+    out, st = _cascade(w, w.shared_prefix_blocks)
+    assert st == pa.PA_OK
+    assert torch.isfinite(out.float()).all()
+    lens = w.seq_lens.cpu().numpy()
+    pick = sorted({0, 1, int(lens.argmax()), int(lens.argmin()), 77, w.num_seqs - 1})
+    rows, ref = oracle_step(w, 0, pick)
+    compare(out, rows, ref, "shared-prefix config, sampled rows")
