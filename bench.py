@@ -491,6 +491,53 @@ def run_reference(args, rank, world):
     }
 
 
+def run_copy_blocks(args, rank, world, local):
+    """Copy-on-write block copies (pa_copy_blocks) on a pool shaped like one layer of the
+    40-layer GQA model (8 KV heads, fp16): `pairs` distinct src -> dst blocks per step."""
+    import paged_kv_cache_99_gb300 as pa
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nb, hkv, pairs = 40_000, 8, 16_384
+    g = torch.Generator(device=dev).manual_seed(1010)
+    k = torch.randn(nb, hkv, W.BLOCK_SIZE, 128, generator=g, device=dev).half()
+    v = torch.randn(nb, hkv, W.BLOCK_SIZE, 128, generator=g, device=dev).half()
+    perm = torch.randperm(nb, generator=g, device=dev).int()
+    src, dst = perm[:pairs].contiguous(), perm[pairs:2 * pairs].contiguous()
+    block_bytes = hkv * W.BLOCK_SIZE * 128 * 2
+    moved = 2 * pairs * block_bytes * 2                  # K and V, read + write
+    for _ in range(args.warmup):
+        pa.pa_copy_blocks(k, v, src, dst)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record()
+        pa.pa_copy_blocks(k, v, src, dst)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world)
+    peaks, peak_src = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    gbs = moved / (ms * 1e-3) / 1e9
+    return {
+        "metric": "copy-on-write block copy GB/s (read + write bytes)",
+        "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+        "config": {"workload": f"copy {pairs} blocks of {hkv} KV heads x 16 x 128 fp16 (K and V) per step, "
+                               f"pool of {nb} blocks ({2 * nb * block_bytes / 1e9:.1f} GB)",
+                   "l2": "inputs larger than L2"},
+        "roofline": {"kernel": "copy_blocks_kernel", "bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, a copy)", "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None, "algorithmic_bytes_per_launch": moved,
+                     "avg_launch_ms": round(ms, 5)},
+        "gpu_launches": args.steps, "clocks": clk,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -501,6 +548,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix workload through pa_decode_shared_prefix (prefix once on the tensor cores)")
+    ap.add_argument("--op", default="attention", choices=["attention", "copy-blocks"],
+                    help="copy-blocks: time the copy-on-write block copies instead of the attention step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
@@ -513,6 +562,8 @@ def main(argv=None):
         dist.init_process_group("nccl")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.op == "copy-blocks":
+        line = run_copy_blocks(args, rank, world, local)
     else:
         line = run_ours(args, rank, world, local)
     if rank == 0 and line is not None:

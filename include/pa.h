@@ -261,6 +261,76 @@ PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache
                                    const float* k_scale, const float* v_scale, pa_stream_t stream);
 
 /*
+ * Block copies for copy-on-write [P1 s.4: a physical block shared by several
+ * block tables carries a reference count; a sequence about to write into a
+ * shared block needs its own copy first].
+ *
+ * For i < num_pairs: block dst[i] <- block src[i], every KV head, in both
+ * caches (layout as pa_decode).  The dst blocks must be distinct and none may be
+ * a src block of the same call (the result is otherwise unspecified).  An id
+ * outside [0, num_blocks) skips its pair and, when workspace is not NULL, is
+ * recorded as PA_ERR_OUT_OF_RANGE in its status word.
+ *
+ *   src, dst        device, int32 [num_pairs]
+ *   workspace       NULL, or a workspace whose status word records errors
+ */
+PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
+                                int num_pairs, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                pa_dtype cache_dtype, void* workspace, pa_stream_t stream);
+
+/*
+ * Block pool (host memory, no GPU work) [P1 s.4 "PagedAttention and Block
+ * Management", s.5 "Prefix Caching"; P3 "The block pool", "Prefix caching is the
+ * second win"].
+ *
+ * A pool of num_blocks physical blocks of block_size tokens.  Block 0 is the
+ * null block and is never handed out, so num_blocks - 1 are usable.  Free blocks
+ * wait in one queue; allocation takes them from the front.  A block in use has
+ * a reference count (one per block table holding it).  A full block of a prompt
+ * is registered under a chained hash (the previous block's hash, its own
+ * tokens, and extra_key at the root of the chain); when its count drops to zero
+ * it keeps that content and goes to the back of the queue (a request's last
+ * blocks ahead of its earlier ones), so later prompts with the same prefix can
+ * reuse it until the front of the queue reaches it.  A block without registered
+ * content goes to the front.  Hits are checked against the stored tokens.
+ *
+ * Functions return PA_ERR_INVALID_ARG for bad arguments (NULL pool, an id that
+ * is not in use where one must be), PA_ERR_OUT_OF_RANGE when the queue holds
+ * too few blocks (then nothing changes).  A pool serialises its own calls.
+ */
+typedef struct pa_block_pool pa_block_pool;
+
+/* NULL for num_blocks < 2, block_size < 1 or no memory. */
+PA_API pa_block_pool* pa_pool_create(int num_blocks, int block_size);
+PA_API void pa_pool_destroy(pa_block_pool* pool);
+/* Blocks in the free queue (with or without reusable content). */
+PA_API int pa_pool_num_free(pa_block_pool* pool);
+/* Blocks holding registered prompt content (in use or free). */
+PA_API int pa_pool_num_cached(pa_block_pool* pool);
+/* Reference count of a block (0 when free), -1 for an id outside the pool. */
+PA_API int pa_pool_ref_count(pa_block_pool* pool, int block);
+/* n blocks for new content (count 1; any content they held is dropped). */
+PA_API pa_status pa_pool_allocate(pa_block_pool* pool, int n, int32_t* blocks);
+/* One more reference to each block (another table aliases it). */
+PA_API pa_status pa_pool_share(pa_block_pool* pool, const int32_t* blocks, int n);
+/* One reference less to each block, given in table order; blocks reaching zero
+ * enter the free queue as described above. */
+PA_API pa_status pa_pool_free(pa_block_pool* pool, const int32_t* blocks, int n);
+/* Blocks for a prompt of num_tokens tokens: ceil(num_tokens / block_size)
+ * entries in `blocks`.  The longest run of leading full blocks whose content is
+ * registered is reused (one more reference each), never including the block
+ * that holds the last token; the rest are allocated, and their full blocks
+ * registered.  *hit_tokens = block_size * reused blocks. */
+PA_API pa_status pa_pool_allocate_prompt(pa_block_pool* pool, const int32_t* tokens, int num_tokens,
+                                         uint64_t extra_key, int32_t* blocks, int* hit_tokens);
+/* Copy-on-write: every blocks[i] with more than one reference is replaced by a
+ * newly allocated block (the shared one loses a reference); the (old, new) pairs
+ * go to src/dst (n entries each at most) for pa_copy_blocks, *num_copies of
+ * them. */
+PA_API pa_status pa_pool_copy_on_write(pa_block_pool* pool, int32_t* blocks, int n, int32_t* src, int32_t* dst,
+                                       int* num_copies);
+
+/*
  * Reads (and clears) the device-side status word of a workspace.  Synchronises
  * `stream`.  Returns PA_OK, PA_ERR_OUT_OF_RANGE or PA_ERR_TIMEOUT (the first
  * recorded, timeouts first), or PA_ERR_CUDA if the copy failed.

@@ -75,6 +75,27 @@ def _lib():
     lib.pa_read_device_status.restype = I
     lib.pa_selftest_wait_timeout.argtypes = [P, Z, ctypes.c_uint, P]
     lib.pa_selftest_wait_timeout.restype = I
+    lib.pa_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.pa_copy_blocks.restype = I
+    lib.pa_pool_create.argtypes = [I, I]
+    lib.pa_pool_create.restype = P
+    lib.pa_pool_destroy.argtypes = [P]
+    lib.pa_pool_destroy.restype = None
+    for name in ("pa_pool_num_free", "pa_pool_num_cached"):
+        getattr(lib, name).argtypes = [P]
+        getattr(lib, name).restype = I
+    lib.pa_pool_ref_count.argtypes = [P, I]
+    lib.pa_pool_ref_count.restype = I
+    lib.pa_pool_allocate.argtypes = [P, I, P]
+    lib.pa_pool_allocate.restype = I
+    lib.pa_pool_share.argtypes = [P, P, I]
+    lib.pa_pool_share.restype = I
+    lib.pa_pool_free.argtypes = [P, P, I]
+    lib.pa_pool_free.restype = I
+    lib.pa_pool_allocate_prompt.argtypes = [P, P, I, ctypes.c_uint64, P, ctypes.POINTER(I)]
+    lib.pa_pool_allocate_prompt.restype = I
+    lib.pa_pool_copy_on_write.argtypes = [P, P, I, P, P, ctypes.POINTER(I)]
+    lib.pa_pool_copy_on_write.restype = I
     _LIB = lib
     return lib
 
@@ -241,3 +262,87 @@ def pa_selftest_wait_timeout(workspace, timeout_us: int, stream=None) -> None:
     _need(workspace, "workspace", (torch.uint8,))
     _check(_lib().pa_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(timeout_us), _stream(stream)),
            "pa_selftest_wait_timeout")
+
+
+def pa_copy_blocks(k_cache, v_cache, src, dst, workspace=None, stream=None):
+    """Copy-on-write block copies: block dst[i] <- src[i] (int32 device tensors) in both caches."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, tuple(_DTYPE))
+    _need(src, "src", (torch.int32,))
+    _need(dst, "dst", (torch.int32,))
+    if src.shape != dst.shape or src.dim() != 1:
+        raise ValueError("src and dst must be 1-D and of equal length")
+    nb, Hkv, bs, d = k_cache.shape
+    st = _lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src), _ptr(dst), int(src.numel()), Hkv, d, bs,
+                               nb, _DTYPE[k_cache.dtype], _ptr(workspace), _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+class BlockPool:
+    """Host block pool (pa_pool_*): free queue with a null block 0, reference counts,
+    prefix caching over chained block hashes, copy-on-write."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        self._lib = _lib()
+        self._p = self._lib.pa_pool_create(int(num_blocks), int(block_size))
+        if not self._p:
+            raise ValueError("pa_pool_create failed")
+        self.block_size = int(block_size)
+
+    def __del__(self):
+        if getattr(self, "_p", None):
+            self._lib.pa_pool_destroy(self._p)
+            self._p = None
+
+    @staticmethod
+    def _ids(blocks):
+        import numpy as np
+        a = np.ascontiguousarray(np.asarray(blocks, dtype=np.int32))
+        return a, a.ctypes.data
+
+    @property
+    def num_free(self) -> int:
+        return self._lib.pa_pool_num_free(self._p)
+
+    @property
+    def num_cached(self) -> int:
+        return self._lib.pa_pool_num_cached(self._p)
+
+    def ref_count(self, block: int) -> int:
+        return self._lib.pa_pool_ref_count(self._p, int(block))
+
+    def allocate(self, n: int) -> list:
+        import numpy as np
+        out = np.zeros(max(int(n), 1), dtype=np.int32)
+        _check(self._lib.pa_pool_allocate(self._p, int(n), out.ctypes.data), "pa_pool_allocate")
+        return out[:int(n)].tolist()
+
+    def share(self, blocks) -> None:
+        a, ptr = self._ids(blocks)
+        _check(self._lib.pa_pool_share(self._p, ptr, a.size), "pa_pool_share")
+
+    def free(self, blocks) -> None:
+        a, ptr = self._ids(blocks)
+        _check(self._lib.pa_pool_free(self._p, ptr, a.size), "pa_pool_free")
+
+    def allocate_prompt(self, tokens, extra_key: int = 0):
+        """-> (blocks, hit_tokens) for a prompt of len(tokens) tokens."""
+        import numpy as np
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        n = -(-t.size // self.block_size)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        hit = ctypes.c_int(0)
+        _check(self._lib.pa_pool_allocate_prompt(self._p, t.ctypes.data, t.size, ctypes.c_uint64(extra_key),
+                                                 out.ctypes.data, ctypes.byref(hit)), "pa_pool_allocate_prompt")
+        return out[:n].tolist(), hit.value
+
+    def copy_on_write(self, blocks):
+        """-> (new_blocks, src, dst): shared blocks replaced by private ones, and the copies to make."""
+        import numpy as np
+        a = np.ascontiguousarray(np.asarray(blocks, dtype=np.int32)).copy()
+        src = np.zeros(max(a.size, 1), dtype=np.int32)
+        dst = np.zeros(max(a.size, 1), dtype=np.int32)
+        c = ctypes.c_int(0)
+        _check(self._lib.pa_pool_copy_on_write(self._p, a.ctypes.data, a.size, src.ctypes.data, dst.ctypes.data,
+                                               ctypes.byref(c)), "pa_pool_copy_on_write")
+        return a.tolist(), src[:c.value].tolist(), dst[:c.value].tolist()

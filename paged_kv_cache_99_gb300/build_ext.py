@@ -11,7 +11,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["pa_api.cu", "decode.cu", "chunk_tc.cu", "reshape_and_cache.cu", "selftest.cu"]
+SOURCES = ["pa_api.cu", "decode.cu", "chunk_tc.cu", "reshape_and_cache.cu", "selftest.cu", "copy_blocks.cu",
+           "pool.cpp"]
 HEADERS = ["pa_device.cuh", "pa_internal.h"]
 BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB_PATH = os.path.join(BUILD_DIR, "libpa.so")
@@ -45,7 +46,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:

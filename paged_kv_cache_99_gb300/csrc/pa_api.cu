@@ -538,6 +538,23 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
                        kNoAllocScratchBytes, 0, num_blocks, cs);
 }
 
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int num_pairs,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks, pa_dtype cache_dtype,
+                         void* workspace, pa_stream_t stream) {
+    if (num_pairs < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype != PA_BF16 && cache_dtype != PA_FP16 && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !src || !dst || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PA_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+    const size_t block_bytes = static_cast<size_t>(num_kv_heads) * kBlockSize * kHeadDim *
+                               (cache_dtype == PA_FP8_E4M3 ? 1 : 2);
+    return cuda_status(launch_copy_blocks(k_cache, v_cache, src, dst, num_pairs, num_blocks, block_bytes,
+                                          static_cast<int*>(workspace), reinterpret_cast<cudaStream_t>(stream)),
+                       "launch(copy_blocks)");
+}
+
 pa_status pa_read_device_status(void* workspace, pa_stream_t stream) {
     if (!workspace) return PA_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -114,6 +114,10 @@ cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas
 cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, const DecodeParams& p, int grid, size_t smem,
                           cudaStream_t stream);
+// Block copies (copy-on-write): dst[i] <- src[i] in both caches.
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int num_pairs,
+                               int num_blocks, size_t block_bytes, int* status, cudaStream_t stream);
+
 cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, int max_ctas,
                            cudaStream_t stream);
 
