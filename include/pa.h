@@ -33,9 +33,10 @@
  *           physical_block * 16 + offset.
  * GQA.      Query head h reads KV head h / (num_q_heads / num_kv_heads):
  *           consecutive query heads form a group [P1 s.2].
- * FP8.      FP8-E4M3 ("fn": bias 7, max 448, no inf, NaN = S.1111.111) with one
- *           float32 scale per tensor, separate for K and V, read from device
- *           memory so that calls can be captured in CUDA graphs.
+ * FP8.      FP8-E4M3 ("fn": bias 7, max 448, no inf, NaN = S.1111.111) with
+ *           float32 scales, separate for K and V, one per tensor (PA_FP8_E4M3) or
+ *           one per KV head (PA_FP8_E4M3_PER_HEAD), read from device memory so
+ *           that calls can be captured in CUDA graphs.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -65,7 +66,15 @@ typedef enum {
     PA_ERR_WORKSPACE = 6
 } pa_status;
 
-typedef enum { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
+/*
+ * Element types.  PA_FP8_E4M3 caches carry one float32 scale per tensor (k_scale,
+ * v_scale point to one float each); PA_FP8_E4M3_PER_HEAD caches hold the same
+ * e4m3 codes with one scale per KV head (k_scale, v_scale point to
+ * num_kv_heads floats, head h's elements dequantised with scale[h]).  The pages
+ * mention an FP8 KV cache [P1 s.7 "--kv-cache-dtype fp8"] but not its scaling;
+ * per-head scales are this library's variant of it.
+ */
+typedef enum { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2, PA_FP8_E4M3_PER_HEAD = 3 } pa_dtype;
 
 /* Static description of a status code.  Never NULL. */
 PA_API const char* pa_status_string(int status);
@@ -97,8 +106,10 @@ PA_API const char* pa_last_error(void);
  *                  binary32 (IEEE division), then round-to-nearest-even to E4M3 with
  *                  magnitudes above 448 clamped to 448; a NaN quotient ->
  *                  S.1111.111 with S the sign bit of the source element x; a zero
- *                  result keeps the quotient's sign [P1 s.2, s.7 "--kv-cache-dtype fp8"].
- *   k_scale,v_scale device float32 scalars; required (non-NULL) iff FP8.
+ *                  result keeps the quotient's sign [P1 s.2, s.7 "--kv-cache-dtype fp8"];
+ *                  or PA_FP8_E4M3_PER_HEAD: the same with head h's scale[h].
+ *   k_scale,v_scale device float32: one each (PA_FP8_E4M3) or num_kv_heads each
+ *                  (PA_FP8_E4M3_PER_HEAD); required (non-NULL) iff FP8.
  * Bytes outside the written slots are never touched.
  */
 PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
@@ -137,7 +148,8 @@ PA_API int pa_default_workers(void);
  *
  *   out            device, [num_seqs][num_q_heads][128] of q_dtype
  *   q              device, [num_seqs][num_q_heads][128], q_dtype bf16|fp16, 16-byte aligned
- *   k_cache,v_cache device, layout above; cache_dtype == q_dtype or PA_FP8_E4M3
+ *   k_cache,v_cache device, layout above; cache_dtype == q_dtype, PA_FP8_E4M3 or
+ *                  PA_FP8_E4M3_PER_HEAD
  *   block_tables   device, int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens       device, int32 [num_seqs]; each <= 16 * max_blocks_per_seq
  *   scale          softmax scale (e.g. 1/sqrt(128))

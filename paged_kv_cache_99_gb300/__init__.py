@@ -17,7 +17,7 @@ from . import build_ext
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_TIMEOUT, PA_ERR_OUT_OF_RANGE, \
     PA_ERR_WORKSPACE = range(7)
-PA_BF16, PA_FP16, PA_FP8_E4M3 = 0, 1, 2
+PA_BF16, PA_FP16, PA_FP8_E4M3, PA_FP8_E4M3_PER_HEAD = 0, 1, 2, 3
 
 _DTYPE = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.uint8: PA_FP8_E4M3,
           torch.float8_e4m3fn: PA_FP8_E4M3}
@@ -118,6 +118,16 @@ def _need(t: torch.Tensor, name: str, dtypes=None):
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
 
 
+def _cache_code(cache, k_scale, num_kv_heads: int) -> int:
+    """pa_dtype of a cache: an e4m3 cache with one scale per KV head is PA_FP8_E4M3_PER_HEAD."""
+    code = _DTYPE[cache.dtype]
+    if code == PA_FP8_E4M3 and k_scale is not None and k_scale.numel() > 1:
+        if k_scale.numel() != num_kv_heads:
+            raise ValueError("FP8 scales must hold one value or one per KV head")
+        return PA_FP8_E4M3_PER_HEAD
+    return code
+
+
 def _check(status: int, what: str) -> None:
     if status != PA_OK:
         raise PagedAttentionError(status, what)
@@ -159,7 +169,7 @@ def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_s
     if v.shape != k.shape or v_cache.shape != k_cache.shape or H2 != H or d2 != d or slot_mapping.shape != (T,):
         raise ValueError("shape mismatch")
     st = _lib().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, H, d,
-                                     bs, nb, _DTYPE[k.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale),
+                                     bs, nb, _DTYPE[k.dtype], _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale),
                                      _ptr(v_scale), _stream(stream))
     _check(st, "pa_reshape_and_cache")
 
@@ -180,7 +190,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, workspace
         raise ValueError("shape mismatch")
     st = _lib().pa_decode_ex(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                              block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, d, bs, nb, float(scale),
-                             _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale), _ptr(v_scale),
+                             _DTYPE[q.dtype], _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale), _ptr(v_scale),
                              _ptr(workspace), workspace.numel(), int(num_workers), _stream(stream))
     _check(st, "pa_decode")
 
@@ -202,7 +212,7 @@ def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, pr
         raise ValueError("shape mismatch")
     st = _lib().pa_decode_shared_prefix(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                         block_tables.shape[1], _ptr(seq_lens), B, int(prefix_blocks), Hq, Hkv, d,
-                                        bs, nb, float(scale), _DTYPE[q.dtype], _DTYPE[k_cache.dtype],
+                                        bs, nb, float(scale), _DTYPE[q.dtype], _cache_code(k_cache, k_scale, k_cache.shape[1]),
                                         _ptr(k_scale), _ptr(v_scale), _ptr(workspace), workspace.numel(),
                                         _stream(stream))
     _check(st, "pa_decode_shared_prefix")
@@ -226,7 +236,7 @@ def pa_mixed(out, q, query_start_loc, k_cache, v_cache, block_tables, seq_lens, 
         raise ValueError("shape mismatch")
     st = _lib().pa_mixed(_ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
                          _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, total_q, int(max_q_len), Hq,
-                         Hkv, d, bs, nb, float(scale), _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale),
+                         Hkv, d, bs, nb, float(scale), _DTYPE[q.dtype], _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale),
                          _ptr(v_scale), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "pa_mixed")
 
@@ -247,7 +257,7 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, scale, k
         raise ValueError("shape mismatch")
     st = _lib().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                   block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, d, bs, nb, float(scale),
-                                  _DTYPE[q.dtype], _DTYPE[k_cache.dtype], _ptr(k_scale), _ptr(v_scale),
+                                  _DTYPE[q.dtype], _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale), _ptr(v_scale),
                                   _stream(stream))
     _check(st, "pa_decode_noalloc")
 

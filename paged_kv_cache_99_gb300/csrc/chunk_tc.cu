@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarQFull));
         }
-        const float kscale = kFp8 ? __ldg(p.k_scale) : 1.0f;
-        const float vscale = kFp8 ? __ldg(p.v_scale) : 1.0f;
+        const float kscale = kFp8 ? __ldg(p.k_scale + h * p.scale_stride) : 1.0f;
+        const float vscale = kFp8 ? __ldg(p.v_scale + h * p.scale_stride) : 1.0f;
         const float s_log2 = p.scale_log2 * kscale;
         const bool pos_scale = s_log2 >= 0.f;
         const uint32_t s_addr = tS(x) + lane_off;

@@ -262,9 +262,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         cursor_advance(P, cum, B, UH);
     }
 
-    const float kscale = kFp8 ? __ldg(p.k_scale) : 1.0f;
-    const float vscale = kFp8 ? __ldg(p.v_scale) : 1.0f;
-    const float s_log2 = p.scale_log2 * kscale;
+    // FP8 scales of the current unit's KV head (set at each segment start)
+    float s_log2 = p.scale_log2, vscale = 1.0f;
 
     Cursor C = start;
     float o[8][4];
@@ -282,6 +281,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
             const int h = C.uh / p.head_groups;
             const int hg = C.uh % p.head_groups;
             const int gh = hg * kHeadsPerGroup + g;        // head within the GQA group
+            if constexpr (kFp8) {
+                s_log2 = p.scale_log2 * __ldg(p.k_scale + h * p.scale_stride);
+                vscale = __ldg(p.v_scale + h * p.scale_stride);
+            }
             const bool live = gh < p.group;
             const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
                                    (static_cast<size_t>(row_cur) * p.num_q_heads + h * p.group + (live ? gh : 0)) * kHeadDim;
@@ -628,7 +631,7 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u) {
             }
         }
     }
-    const float vscale = Fp8Layout ? __ldg(p.v_scale) : 1.0f;
+    const float vscale = Fp8Layout ? __ldg(p.v_scale + h * p.scale_stride) : 1.0f;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int gh = hg * kHeadsPerGroup + 2 * t + e;

@@ -109,6 +109,11 @@ pa_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, i
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+bool is_fp8(pa_dtype d) { return d == PA_FP8_E4M3 || d == PA_FP8_E4M3_PER_HEAD; }
+
+// FP8 scale stride: 0 for one scale per tensor, 1 for one per KV head
+int scale_stride_of(pa_dtype d) { return d == PA_FP8_E4M3_PER_HEAD ? 1 : 0; }
+
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int head_groups_of(int num_q_heads, int num_kv_heads) {
@@ -126,13 +131,13 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
                                const float* k_scale, const float* v_scale, const void* workspace) {
     if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
     if (q_dtype != PA_BF16 && q_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
-    if (cache_dtype != q_dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype != q_dtype && !is_fp8(cache_dtype)) return PA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || num_seqs > kMaxSeqs) return PA_ERR_INVALID_ARG;
     if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (num_blocks <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace) return PA_ERR_INVALID_ARG;
-    if (cache_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    if (is_fp8(cache_dtype) && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(workspace, 256))
         return PA_ERR_INVALID_ARG;
@@ -144,7 +149,7 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
 }
 
 CacheKind kind_of(pa_dtype cache_dtype) {
-    return cache_dtype == PA_FP8_E4M3 ? kKindFp8 : (cache_dtype == PA_FP16 ? kKindFp16 : kKindBf16);
+    return is_fp8(cache_dtype) ? kKindFp8 : (cache_dtype == PA_FP16 ? kKindFp16 : kKindBf16);
 }
 
 pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
@@ -203,6 +208,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.query_start_loc = query_start_loc;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.scale_stride = scale_stride_of(cache_dtype);
     p.status = reinterpret_cast<int*>(ws + lay.status_off);
     p.plan = reinterpret_cast<int*>(ws + lay.plan_off);
     p.ml = reinterpret_cast<float*>(ws + lay.ml_off);
@@ -267,6 +273,7 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.seq_lens = seq_lens;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.scale_stride = scale_stride_of(cache_dtype);
     p.status = static_cast<int*>(workspace);
     p.num_seqs = num_seqs;
     p.num_q_heads = num_q_heads;
@@ -368,17 +375,17 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
                                const float* k_scale, const float* v_scale, pa_stream_t stream) {
     if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
     if (src_dtype != PA_BF16 && src_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
-    if (cache_dtype != src_dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype != src_dtype && !is_fp8(cache_dtype)) return PA_ERR_UNSUPPORTED;
     if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
     if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
-    if (cache_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    if (is_fp8(cache_dtype) && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(slot_mapping, 8))
         return PA_ERR_INVALID_ARG;
     if (static_cast<long long>(num_tokens) * num_kv_heads >= (1ll << 34)) return PA_ERR_UNSUPPORTED;
     return cuda_status(launch_reshape(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, num_blocks,
-                                      src_dtype == PA_BF16, cache_dtype == PA_FP8_E4M3, k_scale, v_scale,
+                                      src_dtype == PA_BF16, is_fp8(cache_dtype), k_scale, v_scale, scale_stride_of(cache_dtype),
                                       reinterpret_cast<cudaStream_t>(stream)),
                        "launch(reshape_and_cache)");
 }
@@ -543,13 +550,13 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const
                          void* workspace, pa_stream_t stream) {
     if (num_pairs < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID_ARG;
     if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
-    if (cache_dtype != PA_BF16 && cache_dtype != PA_FP16 && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype != PA_BF16 && cache_dtype != PA_FP16 && !is_fp8(cache_dtype)) return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
     if (!k_cache || !v_cache || !src || !dst || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PA_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
     const size_t block_bytes = static_cast<size_t>(num_kv_heads) * kBlockSize * kHeadDim *
-                               (cache_dtype == PA_FP8_E4M3 ? 1 : 2);
+                               (is_fp8(cache_dtype) ? 1 : 2);
     return cuda_status(launch_copy_blocks(k_cache, v_cache, src, dst, num_pairs, num_blocks, block_bytes,
                                           static_cast<int*>(workspace), reinterpret_cast<cudaStream_t>(stream)),
                        "launch(copy_blocks)");

@@ -38,6 +38,7 @@ struct DecodeParams {
     const int32_t* query_start_loc;   // non-null: mixed batch, only rows with q_len == 1
     const float* k_scale;
     const float* v_scale;
+    int scale_stride;                 // FP8 scales: 0 one per tensor, 1 one per KV head
     int* status;                      // device status word
     int* plan;                        // [num_seqs + 1]: block prefix per sequence (large batches only)
     float* ml;                        // [slots][16]: running max (8 heads), sum (8 heads)
@@ -75,6 +76,7 @@ struct ChunkParams {
     const int32_t* seq_lens;
     const float* k_scale;
     const float* v_scale;
+    int scale_stride;                 // FP8 scales: 0 one per tensor, 1 one per KV head
     int* status;
     int num_seqs;
     int num_q_heads;
@@ -125,7 +127,7 @@ cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p,
 cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_kv_heads, int num_blocks,
                            bool src_bf16, bool cache_fp8, const float* k_scale,
-                           const float* v_scale, cudaStream_t stream);
+                           const float* v_scale, int scale_stride, cudaStream_t stream);
 
 // Prefill chunks.
 size_t chunk_smem_bytes(CacheKind kind, int num_seqs);

@@ -42,7 +42,7 @@ template <bool SrcBf16, bool Fp8>
 __global__ void __launch_bounds__(256)
     reshape_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, void* k_cache,
                    void* v_cache, const int64_t* __restrict__ slots, int num_tokens, int num_kv_heads,
-                   int num_blocks, const float* k_scale, const float* v_scale) {
+                   int num_blocks, const float* k_scale, const float* v_scale, int scale_stride) {
     grid_dependency_wait();
     grid_launch_dependents();
     const long long pair = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256)
     if constexpr (!Fp8) {
         *reinterpret_cast<uint4*>(static_cast<uint16_t*>(is_v ? v_cache : k_cache) + dst) = x;
     } else {
-        const float scale = __ldg(is_v ? v_scale : k_scale);
+        const float scale = __ldg((is_v ? v_scale : k_scale) + h * scale_stride);   // per tensor or per head
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t out[2];
 #pragma unroll
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_kv_heads, int num_blocks,
                            bool src_bf16, bool cache_fp8, const float* k_scale,
-                           const float* v_scale, cudaStream_t stream) {
+                           const float* v_scale, int scale_stride, cudaStream_t stream) {
     const long long pairs = static_cast<long long>(num_tokens) * num_kv_heads;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((pairs + 7) / 8));
@@ -90,12 +90,12 @@ cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_
     const uint16_t* vv = static_cast<const uint16_t*>(v);
     if (cache_fp8) {
         return src_bf16 ? cudaLaunchKernelEx(&cfg, reshape_kernel<true, true>, kk, vv, k_cache, v_cache, slots,
-                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale)
+                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale, scale_stride)
                         : cudaLaunchKernelEx(&cfg, reshape_kernel<false, true>, kk, vv, k_cache, v_cache, slots,
-                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale);
+                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale, scale_stride);
     }
     return cudaLaunchKernelEx(&cfg, reshape_kernel<true, false>, kk, vv, k_cache, v_cache, slots, num_tokens,
-                              num_kv_heads, num_blocks, k_scale, v_scale);
+                              num_kv_heads, num_blocks, k_scale, v_scale, scale_stride);
 }
 
 }  // namespace pa

@@ -122,7 +122,7 @@ def build_workload(*, name: str, seed: int, device, num_layers: int, seq_lens, q
                    cache_dtype: str = "bf16", extra_blocks: int = 64,
                    shared_prefix_blocks: int = 0, pool_blocks: int | None = None,
                    write_new: bool = True, head_dim: int = HEAD_DIM,
-                   block_size: int = BLOCK_SIZE) -> Workload:
+                   block_size: int = BLOCK_SIZE, fp8_scale: str = "tensor") -> Workload:
     """Build a paged batch.
 
     seq_lens[s] counts the tokens in the cache after this step (context plus the
@@ -195,7 +195,26 @@ def build_workload(*, name: str, seed: int, device, num_layers: int, seq_lens, q
         v_new[layer] = _draw(v_new.shape[1:], src_dtype, vgen, device)
         kc = _draw(shape, cache_dtype if cache_dtype != "fp8" else "bf16", vgen, device)
         vc = _draw(shape, cache_dtype if cache_dtype != "fp8" else "bf16", vgen, device)
-        if cache_dtype == "fp8":
+        if cache_dtype == "fp8" and fp8_scale == "head":
+            # heads of different magnitude (K of head h x 2^(h mod 4), V x 2^((h+1) mod 4)),
+            # so that each head needs its own scale
+            hk = 2.0 ** (torch.arange(num_kv_heads, device=device) % 4).float()
+            hv = 2.0 ** ((torch.arange(num_kv_heads, device=device) + 1) % 4).float()
+            kc = (kc.float() * hk.view(1, -1, 1, 1)).to(kc.dtype)
+            vc = (vc.float() * hv.view(1, -1, 1, 1)).to(vc.dtype)
+            k_new[layer] = (k_new[layer].float() * hk.view(1, -1, 1)).to(k_new.dtype)
+            v_new[layer] = (v_new[layer].float() * hv.view(1, -1, 1)).to(v_new.dtype)
+            # one scale per KV head: amax over that head's bf16 values destined for the cache
+            def head_amax(c, new):
+                m = c.abs().float().amax(dim=(0, 2, 3))
+                return torch.maximum(m, new.abs().float().amax(dim=(0, 2))) if T else m
+            ks = head_amax(kc, k_new[layer]) / 448.0
+            vs = head_amax(vc, v_new[layer]) / 448.0
+            kc = (kc.float() / ks.view(1, -1, 1, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
+            vc = (vc.float() / vs.view(1, -1, 1, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
+            k_scales.append(ks)
+            v_scales.append(vs)
+        elif cache_dtype == "fp8":
             # per-tensor scale: amax over every bf16 value destined for this cache
             ks = torch.maximum(kc.abs().max().float(), k_new[layer].abs().max().float() if T else
                                torch.zeros((), device=device)) / 448.0

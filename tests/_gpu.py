@@ -65,23 +65,38 @@ def oracle_step(w: W.Workload, layer: int = 0, seqs=None):
     sub_qsl[1:] = np.cumsum([qsl[s + 1] - qsl[s] for s in seqs])
     qbits = raw(w.q[layer][torch.as_tensor(rows, device=w.q.device)]) if len(rows) else \
         np.zeros((0, w.num_q_heads, w.head_dim), np.uint16)
-    ks = float(w.k_scale[layer]) if w.k_scale is not None else 1.0
-    vs = float(w.v_scale[layer]) if w.v_scale is not None else 1.0
     cd = CODE[w.cache_dtype]
-    if w.num_new_tokens:
-        # the new tokens of the chosen sequences, with their slots renumbered
-        slots = w.slot_mapping.cpu().numpy()
-        tok_rows = rows  # new tokens are aligned with query rows when the workload writes
-        new_slots = np.array([remap[int(slots[r]) // w.block_size] * w.block_size + int(slots[r]) % w.block_size
-                              for r in tok_rows], np.int64)
-        tsel = torch.as_tensor(tok_rows, device=w.k_new.device)
-        kc, vc = oracle.reshape_and_cache(raw(w.k_new[layer][tsel]), raw(w.v_new[layer][tsel]), CODE[w.q_dtype],
-                                          kc, vc, cd, new_slots, ks, vs)
     sub_lens = lens[seqs].astype(np.int32)
-    if w.is_decode_only:
-        out = oracle.decode(qbits, CODE[w.q_dtype], kc, vc, cd, sub_tables, sub_lens, w.scale, ks, vs)
-    else:
-        out = oracle.mixed(qbits, CODE[w.q_dtype], sub_qsl, kc, vc, cd, sub_tables, sub_lens, w.scale, ks, vs)
+
+    def run(ks, vs):
+        k, v = kc, vc
+        if w.num_new_tokens:
+            # the new tokens of the chosen sequences, with their slots renumbered
+            slots = w.slot_mapping.cpu().numpy()
+            tok_rows = rows  # new tokens are aligned with query rows when the workload writes
+            new_slots = np.array([remap[int(slots[r]) // w.block_size] * w.block_size + int(slots[r]) % w.block_size
+                                  for r in tok_rows], np.int64)
+            tsel = torch.as_tensor(tok_rows, device=w.k_new.device)
+            k, v = oracle.reshape_and_cache(raw(w.k_new[layer][tsel]), raw(w.v_new[layer][tsel]), CODE[w.q_dtype],
+                                            k, v, cd, new_slots, ks, vs)
+        if w.is_decode_only:
+            return oracle.decode(qbits, CODE[w.q_dtype], k, v, cd, sub_tables, sub_lens, w.scale, ks, vs)
+        return oracle.mixed(qbits, CODE[w.q_dtype], sub_qsl, k, v, cd, sub_tables, sub_lens, w.scale, ks, vs)
+
+    if w.k_scale is None:
+        return rows, run(1.0, 1.0)
+    kscales = w.k_scale[layer].reshape(-1).tolist()
+    vscales = w.v_scale[layer].reshape(-1).tolist()
+    if len(kscales) == 1:
+        return rows, run(kscales[0], vscales[0])
+    # one scale per KV head: the outputs of KV head h's query heads depend on its
+    # elements only, so run the oracle once per head with that head's scales
+    G = w.num_q_heads // w.num_kv_heads
+    out = None
+    for h, (ks, vs) in enumerate(zip(kscales, vscales)):
+        o = run(ks, vs)
+        out = o if out is None else out
+        out[:, h * G:(h + 1) * G] = o[:, h * G:(h + 1) * G]
     return rows, out
 
 
