@@ -59,6 +59,25 @@ def kv_read_bytes(w: W.Workload) -> int:
     return w.num_layers * int(w.seq_lens.sum().item()) * 2 * w.num_kv_heads * w.head_dim * ELEM[w.cache_dtype]
 
 
+def describe(name: str, block_size: int) -> str:
+    d = DESCRIPTIONS.get(name, name)
+    if block_size != W.BLOCK_SIZE:
+        d = d.replace("block 16", f"block {block_size}").replace(
+            "128 aliased prefix blocks", f"2048-token aliased prefix ({2048 // block_size} blocks of {block_size})")
+    return d
+
+
+def last_block_waste(w: W.Workload) -> float:
+    """Share of the allocated cache slots that hold no token: the empty tail of
+    every sequence's last block (shared prefix blocks counted once)."""
+    bs = w.block_size
+    lens = [int(n) for n in w.seq_lens.tolist()]
+    pre = w.shared_prefix_blocks * bs
+    used = sum(n - pre for n in lens) + (pre if lens else 0)
+    alloc = sum(-(-(n - pre) // bs) * bs for n in lens) + (pre if lens else 0)
+    return round(1.0 - used / alloc, 5) if alloc else 0.0
+
+
 def chunk_flops(w: W.Workload) -> int:
     """Algorithmic FLOPs of the prefill chunks of one layer: QK^T and PV, 2 per
     multiply-add, over the causal key range of every chunk row (no padding)."""
@@ -220,7 +239,8 @@ def run_ours(args, rank, world, local):
     import paged_kv_cache_99_gb300 as pa
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.make(args.workload, dev)          # every replica runs the same workload (weak scaling)
+    # every replica runs the same workload (weak scaling)
+    w = W.make(args.workload, dev, **({"block_size": args.block_size} if args.block_size != W.BLOCK_SIZE else {}))
     layers_caches = [(w.k_cache[l], w.v_cache[l]) for l in range(w.num_layers)]
     ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, device=dev)
     outs = [torch.empty_like(w.q[l]) for l in range(w.num_layers)]
@@ -313,8 +333,8 @@ def run_ours(args, rank, world, local):
     per_launch_bytes = kv_bytes / w.num_layers
     if cascade:
         # the cascade reads the shared blocks once: its roofline counts unique bytes
-        tok = sum(int(n) - w.shared_prefix_blocks * W.BLOCK_SIZE for n in w.seq_lens.tolist())
-        tok += w.shared_prefix_blocks * W.BLOCK_SIZE
+        tok = sum(int(n) - w.shared_prefix_blocks * w.block_size for n in w.seq_lens.tolist())
+        tok += w.shared_prefix_blocks * w.block_size
         per_launch_bytes = tok * 2 * w.num_kv_heads * w.head_dim * ELEM[w.cache_dtype]
     achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
     traffic = None if cascade else recorded_traffic(args.workload)
@@ -332,8 +352,10 @@ def run_ours(args, rank, world, local):
         "dtype": w.cache_dtype,
         "data": "synthetic",
         "config": {
-            "workload": DESCRIPTIONS.get(args.workload, args.workload),
+            "workload": describe(args.workload, w.block_size),
             "name": args.workload,
+            "block_size": w.block_size,
+            "last_block_waste": last_block_waste(w),
             "kv_bytes_per_step": kv_bytes,
             "launch": f"one CUDA graph per step: {w.num_layers} x ("
                       + ("pa_reshape_and_cache + " if w.num_new_tokens else "")
@@ -471,6 +493,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     kw = {"num_layers": 1} if args.workload in ("qwen2.5-1.5b", "gqa40-8k") else {}
+    if args.block_size != W.BLOCK_SIZE:
+        kw["block_size"] = args.block_size
     w = W.make(args.workload, "cpu", **kw)
     total = {"qwen2.5-1.5b": 28, "gqa40-8k": 40}.get(args.workload, w.num_layers)
     per_step = []
@@ -485,7 +509,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS.get(args.workload, args.workload), "name": args.workload},
+        "config": {"workload": describe(args.workload, w.block_size), "name": args.workload,
+                   "block_size": w.block_size},
         "cpu_baseline": cb,
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -499,11 +524,14 @@ def run_copy_blocks(args, rank, world, local):
     dev = torch.device("cuda", local)
     nb, hkv, pairs = 40_000, 8, 16_384
     g = torch.Generator(device=dev).manual_seed(1010)
-    k = torch.randn(nb, hkv, W.BLOCK_SIZE, 128, generator=g, device=dev).half()
-    v = torch.randn(nb, hkv, W.BLOCK_SIZE, 128, generator=g, device=dev).half()
+    bs = args.block_size
+    nb = nb * W.BLOCK_SIZE // bs                         # the same pool and copied bytes at every block size
+    pairs = pairs * W.BLOCK_SIZE // bs
+    k = torch.randn(nb, hkv, bs, 128, generator=g, device=dev).half()
+    v = torch.randn(nb, hkv, bs, 128, generator=g, device=dev).half()
     perm = torch.randperm(nb, generator=g, device=dev).int()
     src, dst = perm[:pairs].contiguous(), perm[pairs:2 * pairs].contiguous()
-    block_bytes = hkv * W.BLOCK_SIZE * 128 * 2
+    block_bytes = hkv * bs * 128 * 2
     moved = 2 * pairs * block_bytes * 2                  # K and V, read + write
     for _ in range(args.warmup):
         pa.pa_copy_blocks(k, v, src, dst)
@@ -527,7 +555,7 @@ def run_copy_blocks(args, rank, world, local):
         "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
-        "config": {"workload": f"copy {pairs} blocks of {hkv} KV heads x 16 x 128 fp16 (K and V) per step, "
+        "config": {"workload": f"copy {pairs} blocks of {hkv} KV heads x {bs} x 128 fp16 (K and V) per step, "
                                f"pool of {nb} blocks ({2 * nb * block_bytes / 1e9:.1f} GB)",
                    "l2": "inputs larger than L2"},
         "roofline": {"kernel": "copy_blocks_kernel", "bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak,
@@ -550,6 +578,8 @@ def main(argv=None):
                     help="shared-prefix workload through pa_decode_shared_prefix (prefix once on the tensor cores)")
     ap.add_argument("--op", default="attention", choices=["attention", "copy-blocks"],
                     help="copy-blocks: time the copy-on-write block copies instead of the attention step")
+    ap.add_argument("--block-size", type=int, default=W.BLOCK_SIZE, choices=[8, 16, 32],
+                    help="tokens per cache block (the named workloads are built with 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)

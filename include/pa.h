@@ -21,16 +21,18 @@
  * Errors.   Host-checkable problems are reported before anything is launched:
  *           PA_ERR_INVALID_ARG (null pointer, negative count, misaligned buffer,
  *           H_q not a multiple of H_kv, ...), PA_ERR_UNSUPPORTED (head_dim != 128,
- *           block_size != 16, dtype pair not listed), PA_ERR_WORKSPACE (workspace
+ *           block_size not 8, 16 or 32, dtype pair not listed), PA_ERR_WORKSPACE (workspace
  *           too small).  A failed launch returns PA_ERR_CUDA.  Problems only the
  *           device can see (a block-table entry outside the pool, a bounded wait
  *           that ran out) are recorded in the workspace's status word and
  *           returned by pa_read_device_status; kernels never trap.
- * Shapes.   head_dim d = 128 and block_size = 16 only.  Cache layout is
- *           [num_blocks][num_kv_heads][16][128] for both K and V, so one
- *           (block, KV head) tile is 16 x 128 contiguous elements (4 KiB in
- *           bf16/fp16, 2 KiB in FP8).  A slot number is
- *           physical_block * 16 + offset.
+ * Shapes.   head_dim d = 128; block_size bs = 8, 16 (the default the pages
+ *           use) or 32: larger blocks waste more of a sequence's last block,
+ *           smaller ones cut the kernels' contiguous runs [P1 s.11, question 3].
+ *           Cache layout is [num_blocks][num_kv_heads][bs][128] for both K and V,
+ *           so one (block, KV head) tile is bs x 128 contiguous elements (4 KiB
+ *           in bf16/fp16 and 2 KiB in FP8 at bs = 16).  A slot number is
+ *           physical_block * bs + offset.
  * GQA.      Query head h reads KV head h / (num_q_heads / num_kv_heads):
  *           consecutive query heads form a group [P1 s.2].
  * FP8.      FP8-E4M3 ("fn": bias 7, max 448, no inf, NaN = S.1111.111) with
@@ -92,9 +94,9 @@ PA_API const char* pa_last_error(void);
  * changes the shape of the problem"].
  *
  * For every new token t in [0, num_tokens) with slot = slot_mapping[t] >= 0,
- * stores k[t][h][:] into k_cache[slot / 16][h][slot % 16][:] and v[t][h][:]
+ * stores k[t][h][:] into k_cache[slot / bs][h][slot % bs][:] and v[t][h][:]
  * into v_cache at the same place, for every KV head h.  A negative slot is
- * padding and writes nothing.  A slot >= num_blocks * 16 is skipped (nothing is
+ * padding and writes nothing.  A slot >= num_blocks * block_size is skipped (nothing is
  * written).  Two tokens with the same slot in one call: undefined which wins.
  *
  *   k, v           device, [num_tokens][num_kv_heads][128] of src_dtype (bf16|fp16)
@@ -151,7 +153,7 @@ PA_API int pa_default_workers(void);
  *   k_cache,v_cache device, layout above; cache_dtype == q_dtype, PA_FP8_E4M3 or
  *                  PA_FP8_E4M3_PER_HEAD
  *   block_tables   device, int32 [num_seqs][max_blocks_per_seq]
- *   seq_lens       device, int32 [num_seqs]; each <= 16 * max_blocks_per_seq
+ *   seq_lens       device, int32 [num_seqs]; each <= block_size * max_blocks_per_seq
  *   scale          softmax scale (e.g. 1/sqrt(128))
  *   k_scale,v_scale device float32 scalars, required iff cache is FP8 (dequant
  *                  is code * scale)
@@ -188,9 +190,12 @@ PA_API pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, con
  * it (the cascade split below is this library's).
  *
  * Precondition: for every sequence s, block_tables[s][j] == block_tables[0][j]
- * for j < prefix_blocks, and seq_lens[s] >= 16 * prefix_blocks.  A batch that
- * violates it is recorded as PA_ERR_OUT_OF_RANGE in the workspace status word
- * (its outputs are then unspecified).
+ * for j < prefix_blocks, and seq_lens[s] >= block_size * prefix_blocks.  A batch
+ * that violates it is recorded as PA_ERR_OUT_OF_RANGE in the workspace status
+ * word (its outputs are then unspecified).  The split between the shared part
+ * and the private parts falls on a multiple of 16 keys: with 8-token blocks and
+ * an odd prefix_blocks the last shared block is read with each sequence's
+ * private blocks (and is not checked against the precondition).
  *
  * The prefix keys are read once for the whole batch: every decode row of every
  * sequence is contracted against them on the tensor cores as one dense tile

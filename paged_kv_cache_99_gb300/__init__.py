@@ -158,7 +158,7 @@ def new_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, device=Non
 
 
 def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None, stream=None):
-    """Slot write: k, v [T, H_kv, 128] -> caches [num_blocks, H_kv, 16, 128] at slot_mapping[T] (int64)."""
+    """Slot write: k, v [T, H_kv, 128] -> caches [num_blocks, H_kv, bs, 128] (bs = 8, 16, 32) at slot_mapping[T] (int64)."""
     for t, n in ((k, "k"), (v, "v")):
         _need(t, n, (torch.bfloat16, torch.float16))
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):

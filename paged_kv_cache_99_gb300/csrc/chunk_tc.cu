@@ -43,7 +43,6 @@ namespace {
 
 constexpr int kTcRows = 128;                 // MMA M of one tile
 constexpr int kTcKeys = 128;                 // keys per step (MMA N of S, K of P.V)
-constexpr int kTcBlocksPerStep = kTcKeys / kBlockSize;
 constexpr int kTcStages = 2;
 constexpr uint32_t kQHalf = 16384;           // Q tile: [128 rows][64 elements] per d-half
 constexpr uint32_t kKvHalf = 16384;          // K or V of a step: [128 keys][64 elements] per d-half
@@ -203,7 +202,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         q0 = p.query_start_loc[s];
         q_len = p.query_start_loc[s + 1] - q0;
         n = p.seq_lens[s];
-        if (n - q_len < 0 || n > p.max_blocks * kBlockSize) {   // inconsistent lengths
+        if (n - q_len < 0 || n > p.max_blocks * p.block_size) {   // inconsistent lengths
             if (threadIdx.x == 0) atomicOr(p.status, kDevErrRange);
             return;
         }
@@ -215,7 +214,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         q_len = B;
         n = p.prefix_keys;
         if (2 * pair * QT >= B) return;
-        if (n > p.max_blocks * kBlockSize) {
+        if (n > p.max_blocks * p.block_size) {
             if (threadIdx.x == 0) atomicOr(p.status, kDevErrRange);
             return;
         }
@@ -234,7 +233,6 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     const int pos_last_cta = qpos(jl1);
     const int nsteps = pos_last_cta / kTcKeys + 1;
     const int nsteps_a = qpos(jl0) / kTcKeys + 1;
-    const int nblocks = pos_last_cta / kBlockSize + 1;
     const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
     auto tile_steps = [&](int x) -> int { return x == 0 ? nsteps_a : (has_b ? nsteps : 0); };
 
@@ -249,47 +247,54 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     bool ok = true;
 
     if (!kFp8 && warp == 0) {
-        // ================= producer (16-bit caches): lane b < 8 copies block b of a step =================
+        // ================= producer (16-bit caches) =================
+        // A step's keys arrive as pieces of R = min(block size, 16) rows, one per lane:
+        // piece c of the step holds keys c R .. c R + R - 1, read from table entry
+        // key / bs at row key mod bs, and lands in rows c R.. of each d-half.
         {
+            const int bsh = p.block_shift;
+            const int rsh = min(bsh, 4);                          // log2(R)
+            const int per_step = kTcKeys >> rsh;                  // pieces per step: 8 or 16
+            const int npieces = (pos_last_cta >> rsh) + 1;        // pieces up to the CTA's last key
             auto entry = [&](int i) -> int {
-                const int j = i * kTcBlocksPerStep + lane;
-                int phys = 0;
-                if (lane < kTcBlocksPerStep && j < nblocks) {
-                    phys = __ldg(bt + j);
+                const int c = i * per_step + lane;
+                int y = 0;
+                if (lane < per_step && c < npieces) {
+                    const int key = c << rsh;
+                    int phys = __ldg(bt + (key >> bsh));
                     if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
                         atomicOr(p.status, kDevErrRange);
                         phys = 0;
                     }
+                    y = ((phys * p.num_kv_heads + h) << bsh) + (key & (p.block_size - 1));
                 }
-                return phys;
+                return y;
             };
-            // block b -> rows 16b..16b+15 of each d-half of the stage
-            auto copy = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int nb, int phys) {
-                if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb) * 2 * 2048);
+            auto copy = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int np, int y) {
+                if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(np) * 2 * (128u << rsh));
                 __syncwarp();
-                if (lane < nb) {
-                    const int y = (phys * p.num_kv_heads + h) * kBlockSize;
-                    tma_load_2d(dst + lane * 2048, map, 0, y, full);
-                    tma_load_2d(dst + kKvHalf + lane * 2048, map, 64, y, full);
+                if (lane < np) {
+                    tma_load_2d(dst + (lane << rsh) * 128, map, 0, y, full);
+                    tma_load_2d(dst + kKvHalf + (lane << rsh) * 128, map, 64, y, full);
                 }
             };
-            int phys = entry(0);
+            int y = entry(0);
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int st = i % kTcStages;
                 const uint32_t par = ((i / kTcStages) - 1) & 1;
-                const int phys_next = i + 1 < nsteps ? entry(i + 1) : 0;
-                const int nb = min(kTcBlocksPerStep, nblocks - i * kTcBlocksPerStep);
+                const int y_next = i + 1 < nsteps ? entry(i + 1) : 0;
+                const int nb = min(per_step, npieces - i * per_step);
                 if (i >= kTcStages && !warp_wait(bar(kBarKEmpty + st), par, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                copy(&kmap, sbase + kOffK + st * kKvBytes, bar(kBarKFull + st), nb, phys);
+                copy(&kmap, sbase + kOffK + st * kKvBytes, bar(kBarKFull + st), nb, y);
                 if (i >= kTcStages && !warp_wait(bar(kBarVEmpty + st), par, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                copy(&vmap, sbase + kOffV + st * kKvBytes, bar(kBarVFull + st), nb, phys);
-                phys = phys_next;
+                copy(&vmap, sbase + kOffV + st * kKvBytes, bar(kBarVFull + st), nb, y);
+                y = y_next;
             }
             if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
         }
@@ -574,12 +579,13 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         auto load_item = [&](const uint8_t* cache, int i, int u, uint4 (&x8)[8]) {
             const int key = i * kTcKeys + 64 * u + krow;
             if (i < nsteps && key <= pos_last_cta) {      // later keys get P = 0: store zeros
-                int phys = __ldg(bt + (key >> 4));
+                int phys = __ldg(bt + (key >> p.block_shift));
                 if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
                     atomicOr(p.status, kDevErrRange);
                     phys = 0;
                 }
-                const size_t off = ((static_cast<size_t>(phys) * p.num_kv_heads + h) * kBlockSize + (key & 15)) * kHeadDim;
+                const size_t off = (((static_cast<size_t>(phys) * p.num_kv_heads + h) << p.block_shift) +
+                                    (key & (p.block_size - 1))) * kHeadDim;
                 const uint4* src = reinterpret_cast<const uint4*>(cache + off);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x8[e] = __ldg(src + e);

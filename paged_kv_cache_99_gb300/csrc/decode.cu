@@ -80,10 +80,13 @@ __device__ __forceinline__ bool decode_row(const DecodeParams& p, int s) {
 
 // Blocks sequence s contributes to the flattened order (its blocks x units); a
 // cascade decode covers only the blocks after the shared prefix.
+// The flattened order counts 16-key units (one MMA tile each) whatever the
+// physical block size: a 32-token block holds two units, an 8-token block half of one.
 __device__ __forceinline__ int unit_blocks_of(const DecodeParams& p, int s, int UH) {
     if (!decode_row(p, s)) return 0;
     const int nb = (max(p.seq_lens[s], 0) + kBlockSize - 1) / kBlockSize;
-    return max(min(nb, p.max_blocks) - p.first_block, 0) * UH;
+    const int cap = (p.max_blocks * p.block_size + kBlockSize - 1) / kBlockSize;
+    return max(min(nb, cap) - p.first_block, 0) * UH;
 }
 
 template <typename T>
@@ -158,12 +161,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     if (p.cascade) {
         // every table must start with sequence 0's first_block entries and every
         // sequence must hold the whole prefix
-        const long long checks = static_cast<long long>(B) * p.first_block;
+        const int shared = (p.first_block * kBlockSize) >> p.block_shift;   // shared table entries
+        const long long checks = static_cast<long long>(B) * shared;
         for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < checks;
              i += static_cast<long long>(gridDim.x) * blockDim.x) {
-            const int s = static_cast<int>(i / p.first_block), j = static_cast<int>(i % p.first_block);
+            const int s = static_cast<int>(i / shared), j = static_cast<int>(i % shared);
             if (__ldg(p.block_tables + static_cast<size_t>(s) * p.max_blocks + j) != __ldg(p.block_tables + j) ||
-                (j == 0 && p.seq_lens[s] < p.first_block * kBlockSize))
+                (j == 0 && p.seq_lens[s] < p.first_block * kBlockSize))   // first_block: 16-key units
                 atomicOr(p.status, kDevErrRange);
         }
     }
@@ -171,7 +175,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     for (int s = blockIdx.x; s < B; s += gridDim.x) {
         if (!eligible(s)) continue;
         const int n = p.seq_lens[s];
-        if (threadIdx.x == 0 && n > p.max_blocks * kBlockSize) atomicOr(p.status, kDevErrRange);
+        if (threadIdx.x == 0 && n > p.max_blocks * p.block_size) atomicOr(p.status, kDevErrRange);
         if (n > 0) continue;
         const int row = mixed ? p.query_start_loc[s] : s;
         uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
@@ -222,35 +226,69 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
 
     // ---- producer: block-table window + TMA issue ----
     int tbl_s = -1, tbl_j0 = -1, tbl = 0;
+    int pn_s = -1, pn_ent = 0;                  // producer: sequence whose table entries are counted
     auto issue = [&](const Cursor& c, int k) {
-        const int ja = c.j + p.first_block;      // table index of the cursor's block
-        if (c.s != tbl_s || (ja & ~31) != tbl_j0) {
-            tbl_s = c.s;
-            tbl_j0 = ja & ~31;
-            const int jj = tbl_j0 + lane;
-            tbl = jj < c.nb + p.first_block ? __ldg(p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + jj) : 0;
+        // unit ja (16 keys) of the sequence: with blocks of 16 or 32 tokens it lies in
+        // table entry 16 ja / bs at row offset 16 ja mod bs; with 8-token blocks it
+        // spans entries 2 ja and 2 ja + 1 (the second only if the sequence reaches it)
+        const int ja = c.j + p.first_block;
+        const int bs = p.block_size, bsh = p.block_shift;
+        if (c.s != pn_s) {
+            pn_s = c.s;
+            pn_ent = (max(p.seq_lens[c.s], 0) + bs - 1) >> bsh;
         }
-        int phys = shfl(tbl, ja & 31);
-        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+        const int ti = (ja * kBlockSize) >> bsh;
+        if (c.s != tbl_s || (ti & ~31) != tbl_j0) {
+            tbl_s = c.s;
+            tbl_j0 = ti & ~31;
+            const int jj = tbl_j0 + lane;
+            tbl = jj < pn_ent && jj < p.max_blocks ? __ldg(p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + jj) : 0;
+        }
+        const bool two = bs < kBlockSize && ti + 1 < pn_ent;
+        int phys0 = shfl(tbl, ti & 31), phys1 = shfl(tbl, (ti + 1) & 31);
+        if (static_cast<unsigned>(phys0) >= static_cast<unsigned>(p.num_blocks) ||
+            (two && static_cast<unsigned>(phys1) >= static_cast<unsigned>(p.num_blocks))) {
             if (lane == 0) atomicOr(p.status, kDevErrRange);
-            phys = 0;
+            phys0 = static_cast<unsigned>(phys0) >= static_cast<unsigned>(p.num_blocks) ? 0 : phys0;
+            phys1 = static_cast<unsigned>(phys1) >= static_cast<unsigned>(p.num_blocks) ? 0 : phys1;
         }
         const int h = c.uh / p.head_groups;
-        const int y = (phys * p.num_kv_heads + h) * kBlockSize;
+        const int y0 = ((phys0 * p.num_kv_heads + h) << bsh) + ((ja * kBlockSize) & (bs - 1));
+        const int y1 = (phys1 * p.num_kv_heads + h) << bsh;
         if (lane == 0) {
             const int st = k % NS;
             const uint32_t bar = my_bars + 8 * st;
             const uint32_t dst = my_tiles + st * STAGE;
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, STAGE);
-            if constexpr (kFp8) {
-                tma_load_2d(dst, &kmap, 0, y, bar);
-                tma_load_2d(dst + TILE, &vmap, 0, y, bar);
+            if (bs >= kBlockSize) {
+                mbar_arrive_expect_tx(bar, STAGE);
+                if constexpr (kFp8) {
+                    tma_load_2d(dst, &kmap, 0, y0, bar);
+                    tma_load_2d(dst + TILE, &vmap, 0, y0, bar);
+                } else {
+                    tma_load_2d(dst, &kmap, 0, y0, bar);
+                    tma_load_2d(dst + 2048, &kmap, 64, y0, bar);
+                    tma_load_2d(dst + TILE, &vmap, 0, y0, bar);
+                    tma_load_2d(dst + TILE + 2048, &vmap, 64, y0, bar);
+                }
             } else {
-                tma_load_2d(dst, &kmap, 0, y, bar);
-                tma_load_2d(dst + 2048, &kmap, 64, y, bar);
-                tma_load_2d(dst + TILE, &vmap, 0, y, bar);
-                tma_load_2d(dst + TILE + 2048, &vmap, 64, y, bar);
+                // 8-row boxes: rows 0-7 of the tile from the first block, 8-15 from the second
+                mbar_arrive_expect_tx(bar, two ? STAGE : STAGE / 2);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    if (e == 1 && !two) break;
+                    const int y = e ? y1 : y0;
+                    const uint32_t o = 1024u * e;
+                    if constexpr (kFp8) {
+                        tma_load_2d(dst + o, &kmap, 0, y, bar);
+                        tma_load_2d(dst + TILE + o, &vmap, 0, y, bar);
+                    } else {
+                        tma_load_2d(dst + o, &kmap, 0, y, bar);
+                        tma_load_2d(dst + 2048 + o, &kmap, 64, y, bar);
+                        tma_load_2d(dst + TILE + o, &vmap, 0, y, bar);
+                        tma_load_2d(dst + TILE + 2048 + o, &vmap, 64, y, bar);
+                    }
+                }
             }
         }
     };

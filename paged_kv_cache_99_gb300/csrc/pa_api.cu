@@ -87,14 +87,16 @@ bool encode_fn() {
 }
 
 // Tensor map over a cache viewed as rows of 128 elements (one token of one KV
-// head); boxes of 16 rows, 128-byte swizzle.  16-bit caches are copied in two
-// 64-element halves, FP8 caches in one 128-byte box.
-pa_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads, bool fp8) {
+// head); boxes of min(block size, 16) rows, 128-byte swizzle.  16-bit caches are
+// copied in two 64-element halves, FP8 caches in one 128-byte box.
+pa_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads, int block_size,
+                           bool fp8) {
     if (!encode_fn()) return PA_ERR_CUDA;
-    const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * num_kv_heads * kBlockSize;
+    const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * num_kv_heads * block_size;
     const cuuint64_t dims[2] = {kHeadDim, rows};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * (fp8 ? 1 : 2)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8 ? 128 : 64), kBlockSize};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8 ? 128 : 64),
+                               static_cast<cuuint32_t>(block_size < kBlockSize ? block_size : kBlockSize)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -108,6 +110,11 @@ pa_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, i
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Tokens per physical block: 8, 16 or 32 (the kernels work in 16-key units).
+bool block_size_ok(int bs) { return bs == 8 || bs == 16 || bs == 32; }
+
+int block_shift_of(int bs) { return bs == 8 ? 3 : (bs == 16 ? 4 : 5); }
 
 bool is_fp8(pa_dtype d) { return d == PA_FP8_E4M3 || d == PA_FP8_E4M3_PER_HEAD; }
 
@@ -129,7 +136,7 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
                                const float* k_scale, const float* v_scale, const void* workspace) {
-    if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (head_dim != kHeadDim || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     if (q_dtype != PA_BF16 && q_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
     if (cache_dtype != q_dtype && !is_fp8(cache_dtype)) return PA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || num_seqs > kMaxSeqs) return PA_ERR_INVALID_ARG;
@@ -141,10 +148,11 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(workspace, 256))
         return PA_ERR_INVALID_ARG;
-    // tensor-map rows and flattened block counts must fit in 32 bits
-    const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * kBlockSize;
+    // tensor-map rows and flattened 16-key unit counts must fit in 32 bits
+    const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
     const long long units = static_cast<long long>(num_seqs) * num_kv_heads * head_groups_of(num_q_heads, num_kv_heads);
-    if (rows >= (1ll << 31) || units * max_blocks_per_seq >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    const long long per_seq = (static_cast<long long>(max_blocks_per_seq) * block_size + kBlockSize - 1) / kBlockSize;
+    if (rows >= (1ll << 31) || units * per_seq >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 
@@ -156,7 +164,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
                       const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
                       const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads, float scale,
                       pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
-                      void* workspace, size_t workspace_bytes, int num_workers, int num_blocks,
+                      void* workspace, size_t workspace_bytes, int num_workers, int num_blocks, int block_size,
                       cudaStream_t stream, bool overlap_prior = false, bool cascade = false,
                       int first_block = 0) {
     int dev = 0;
@@ -194,9 +202,9 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     if (workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
 
     CUtensorMap kmap, vmap;
-    pa_status s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+    pa_status s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, kind == kKindFp8);
     if (s != PA_OK) return s;
-    s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+    s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, kind == kKindFp8);
     if (s != PA_OK) return s;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -220,6 +228,8 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.head_groups = hg;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.block_shift = block_shift_of(block_size);
     p.num_workers = W;
     p.overlap_prior = overlap_prior ? 1 : 0;
     p.cascade = cascade ? 1 : 0;
@@ -238,9 +248,9 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
                      const void* v_cache, const CUtensorMap& kmap, const CUtensorMap& vmap,
                      const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* seq_lens, int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
-                     int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
-                     const float* v_scale, void* workspace, cudaStream_t stream, int prefix_blocks = 0,
-                     float* prefix_o = nullptr, float* prefix_ml = nullptr) {
+                     int num_blocks, int block_size, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                     const float* k_scale, const float* v_scale, void* workspace, cudaStream_t stream,
+                     int prefix_units = 0, float* prefix_o = nullptr, float* prefix_ml = nullptr) {
     DeviceState* st = device_state(nullptr);
     if (!st) return PA_ERR_CUDA;
     const CacheKind kind = kind_of(cache_dtype);
@@ -260,7 +270,7 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     }
     const int per_cta = qt * chunk_tiles_per_cta();   // queries of one chunk per CTA
     // prefix mode: the queries are the sequences' decode rows, one tile pair per CTA
-    const long long grid_x = prefix_blocks > 0 ? (num_seqs + per_cta - 1) / per_cta
+    const long long grid_x = prefix_units > 0 ? (num_seqs + per_cta - 1) / per_cta
                                                : static_cast<long long>(num_seqs) + (total_q + per_cta - 1) / per_cta;
     if (grid_x >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     ChunkParams p;
@@ -281,8 +291,10 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.group = group;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.block_shift = block_shift_of(block_size);
     p.queries_per_tile = qt;
-    p.prefix_keys = prefix_blocks * kBlockSize;
+    p.prefix_keys = prefix_units * kBlockSize;
     p.prefix_o = prefix_o;
     p.prefix_ml = prefix_ml;
     p.scale_log2 = scale * 1.4426950408889634f;
@@ -373,7 +385,7 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
                                const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
                                int block_size, int num_blocks, pa_dtype src_dtype, pa_dtype cache_dtype,
                                const float* k_scale, const float* v_scale, pa_stream_t stream) {
-    if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (head_dim != kHeadDim || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     if (src_dtype != PA_BF16 && src_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
     if (cache_dtype != src_dtype && !is_fp8(cache_dtype)) return PA_ERR_UNSUPPORTED;
     if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
@@ -385,7 +397,7 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
         return PA_ERR_INVALID_ARG;
     if (static_cast<long long>(num_tokens) * num_kv_heads >= (1ll << 34)) return PA_ERR_UNSUPPORTED;
     return cuda_status(launch_reshape(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, num_blocks,
-                                      src_dtype == PA_BF16, is_fp8(cache_dtype), k_scale, v_scale, scale_stride_of(cache_dtype),
+                                      block_shift_of(block_size), src_dtype == PA_BF16, is_fp8(cache_dtype), k_scale, v_scale, scale_stride_of(cache_dtype),
                                       reinterpret_cast<cudaStream_t>(stream)),
                        "launch(reshape_and_cache)");
 }
@@ -419,7 +431,7 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void
     if (num_seqs == 0) return PA_OK;
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
-                       workspace_bytes, num_workers, num_blocks, reinterpret_cast<cudaStream_t>(stream));
+                       workspace_bytes, num_workers, num_blocks, block_size, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -436,27 +448,30 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
     if (num_seqs == 0) return PA_OK;
     if (workspace_bytes < pa_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)) return PA_ERR_WORKSPACE;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (prefix_blocks > 0) {
+    // the split runs at a 16-key boundary: with 8-token blocks an odd last shared
+    // block goes to every sequence's own part
+    const int prefix_units = static_cast<int>(static_cast<long long>(prefix_blocks) * block_size / kBlockSize);
+    if (prefix_units > 0) {
         // the shared prefix once, as a dense contraction of every decode row against its keys
         const CacheKind kind = kind_of(cache_dtype);
         CUtensorMap kmap, vmap;
-        s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, kind == kKindFp8);
         if (s != PA_OK) return s;
-        s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, kind == kKindFp8);
         if (s != PA_OK) return s;
         const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads,
                                                             head_groups_of(num_q_heads, num_kv_heads), 0);
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         s = chunk_impl(out, q, nullptr, k_cache, v_cache, kmap, vmap, block_tables, max_blocks_per_seq, seq_lens,
-                       num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, q_dtype, cache_dtype,
-                       k_scale, v_scale, workspace, cs, prefix_blocks,
+                       num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, block_size, scale, q_dtype,
+                       cache_dtype, k_scale, v_scale, workspace, cs, prefix_units,
                        reinterpret_cast<float*>(ws + lay.prefix_o_off), reinterpret_cast<float*>(ws + lay.prefix_ml_off));
         if (s != PA_OK) return s;
     }
     // the private suffixes stream beside it, on the SMs the prefix grid leaves free;
     // the combine merges both
     int workers = 0;
-    if (prefix_blocks > 0) {
+    if (prefix_units > 0) {
         DeviceState* st = device_state(nullptr);
         if (!st) return PA_ERR_CUDA;
         const int per_cta = (chunk_rows() / (num_q_heads / num_kv_heads)) * chunk_tiles_per_cta();
@@ -466,7 +481,7 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
     }
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
-                       workspace_bytes, workers, num_blocks, cs, prefix_blocks > 0, true, prefix_blocks);
+                       workspace_bytes, workers, num_blocks, block_size, cs, prefix_units > 0, true, prefix_units);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -496,12 +511,12 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
     if (chunks) {
         const CacheKind kind = kind_of(cache_dtype);
         CUtensorMap kmap, vmap;
-        s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        s = encode_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, kind == kKindFp8);
         if (s != PA_OK) return s;
-        s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, kind == kKindFp8);
+        s = encode_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, kind == kKindFp8);
         if (s != PA_OK) return s;
         s = chunk_impl(out, q, query_start_loc, k_cache, v_cache, kmap, vmap, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
-                       total_q, num_q_heads, num_kv_heads, num_blocks, scale, q_dtype, cache_dtype, k_scale,
+                       total_q, num_q_heads, num_kv_heads, num_blocks, block_size, scale, q_dtype, cache_dtype, k_scale,
                        v_scale, workspace, cs);
         if (s != PA_OK) return s;
     }
@@ -510,7 +525,7 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
     // chunk grid leaves idle
     return decode_impl(out, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                        num_seqs, num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale,
-                       workspace, workspace_bytes, 0, num_blocks, cs, chunks);
+                       workspace, workspace_bytes, 0, num_blocks, block_size, cs, chunks);
 }
 
 pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -542,20 +557,20 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
     if (s != PA_OK) return s;
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, scratch,
-                       kNoAllocScratchBytes, 0, num_blocks, cs);
+                       kNoAllocScratchBytes, 0, num_blocks, block_size, cs);
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int num_pairs,
                          int num_kv_heads, int head_dim, int block_size, int num_blocks, pa_dtype cache_dtype,
                          void* workspace, pa_stream_t stream) {
     if (num_pairs < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID_ARG;
-    if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (head_dim != kHeadDim || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     if (cache_dtype != PA_BF16 && cache_dtype != PA_FP16 && !is_fp8(cache_dtype)) return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
     if (!k_cache || !v_cache || !src || !dst || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PA_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
-    const size_t block_bytes = static_cast<size_t>(num_kv_heads) * kBlockSize * kHeadDim *
+    const size_t block_bytes = static_cast<size_t>(num_kv_heads) * block_size * kHeadDim *
                                (is_fp8(cache_dtype) ? 1 : 2);
     return cuda_status(launch_copy_blocks(k_cache, v_cache, src, dst, num_pairs, num_blocks, block_bytes,
                                           static_cast<int*>(workspace), reinterpret_cast<cudaStream_t>(stream)),

@@ -11,6 +11,8 @@ namespace pa {
 enum CacheKind { kKindBf16 = 0, kKindFp16 = 1, kKindFp8 = 2 };
 
 constexpr int kHeadDim = 128;
+// Keys per MMA unit: the attention kernels walk the cache in 16-key units, whatever
+// the physical block size (8, 16 or 32 tokens: half a unit, one, or two).
 constexpr int kBlockSize = 16;
 constexpr int kMaxSeqs = 8192;
 constexpr int kDecodeWarps = 4;        // warps per decode CTA
@@ -50,6 +52,8 @@ struct DecodeParams {
     int head_groups;                  // ceil(group / 8)
     int max_blocks;                   // block-table row length
     int num_blocks;                   // pool size
+    int block_size;                   // tokens per physical block: 8, 16 or 32
+    int block_shift;                  // log2(block_size)
     int num_workers;                  // warps taking part
     int overlap_prior;                // nonzero: the previous launch is this call's chunk kernel,
                                       // which started only after its own predecessors finished;
@@ -58,7 +62,7 @@ struct DecodeParams {
     // physical blocks; the decode grid covers blocks first_block.. only and always
     // leaves partials, and the combine folds in the prefix partial of each row.
     int cascade;                      // nonzero: cascade mode
-    int first_block;                  // shared leading blocks (cascade mode)
+    int first_block;                  // shared leading 16-key units (cascade mode)
     const float* prefix_o;            // [num_seqs][num_q_heads][128]: unnormalised prefix output
     const float* prefix_ml;           // [num_seqs][num_q_heads][2]: its (max in log2 units, sum)
     float scale_log2;                 // softmax scale * log2(e)
@@ -84,6 +88,8 @@ struct ChunkParams {
     int group;
     int max_blocks;
     int num_blocks;
+    int block_size;                   // tokens per physical block: 8, 16 or 32
+    int block_shift;                  // log2(block_size)
     int queries_per_tile;             // queries of one sequence per CTA tile
     // Prefix mode (prefix_keys > 0): the queries are the decode rows of all
     // sequences ([num_seqs][num_q_heads][128]), every one at position prefix_keys - 1,
@@ -126,7 +132,7 @@ cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p,
 // Slot write.
 cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_kv_heads, int num_blocks,
-                           bool src_bf16, bool cache_fp8, const float* k_scale,
+                           int block_shift, bool src_bf16, bool cache_fp8, const float* k_scale,
                            const float* v_scale, int scale_stride, cudaStream_t stream);
 
 // Prefill chunks.

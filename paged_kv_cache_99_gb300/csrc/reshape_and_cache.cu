@@ -1,9 +1,10 @@
 // Slot write ("reshape_and_cache") for sm_103a.
 //
 // Every new token's K and V vectors (one per KV head) go to the cache slot the
-// slot mapping names: physical block slot / 16, offset slot % 16 ("Basics of
-// LLM Inference and vLLM Internals", s.4: a block table maps logical blocks to
-// physical blocks; the slot mapping is that table resolved per token).
+// slot mapping names: physical block slot / bs, offset slot % bs for blocks of
+// bs = 8, 16 or 32 tokens ("Basics of LLM Inference and vLLM Internals", s.4: a
+// block table maps logical blocks to physical blocks; the slot mapping is that
+// table resolved per token).
 //
 // One warp per (token, KV head): lanes 0-15 move the 256-byte K row, lanes
 // 16-31 the V row, 16 bytes per lane.  An FP8 cache stores
@@ -42,7 +43,7 @@ template <bool SrcBf16, bool Fp8>
 __global__ void __launch_bounds__(256)
     reshape_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, void* k_cache,
                    void* v_cache, const int64_t* __restrict__ slots, int num_tokens, int num_kv_heads,
-                   int num_blocks, const float* k_scale, const float* v_scale, int scale_stride) {
+                   int num_blocks, int block_shift, const float* k_scale, const float* v_scale, int scale_stride) {
     grid_dependency_wait();
     grid_launch_dependents();
     const long long pair = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -50,12 +51,13 @@ __global__ void __launch_bounds__(256)
     const int tok = static_cast<int>(pair / num_kv_heads);
     const int h = static_cast<int>(pair % num_kv_heads);
     const long long slot = slots[tok];
-    if (slot < 0 || slot >= static_cast<long long>(num_blocks) * kBlockSize) return;
+    if (slot < 0 || slot >= (static_cast<long long>(num_blocks) << block_shift)) return;
     const int lane = threadIdx.x & 31;
     const bool is_v = lane >= 16;
     const int col = (lane & 15) * 8;
     const uint16_t* src = (is_v ? v : k) + (static_cast<size_t>(tok) * num_kv_heads + h) * kHeadDim + col;
-    const size_t dst = ((static_cast<size_t>(slot >> 4) * num_kv_heads + h) * kBlockSize + (slot & 15)) * kHeadDim + col;
+    const size_t dst = (((static_cast<size_t>(slot >> block_shift) * num_kv_heads + h) << block_shift) +
+                        static_cast<size_t>(slot & ((1 << block_shift) - 1))) * kHeadDim + col;
     const uint4 x = *reinterpret_cast<const uint4*>(src);
     if constexpr (!Fp8) {
         *reinterpret_cast<uint4*>(static_cast<uint16_t*>(is_v ? v_cache : k_cache) + dst) = x;
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_kv_heads, int num_blocks,
-                           bool src_bf16, bool cache_fp8, const float* k_scale,
+                           int block_shift, bool src_bf16, bool cache_fp8, const float* k_scale,
                            const float* v_scale, int scale_stride, cudaStream_t stream) {
     const long long pairs = static_cast<long long>(num_tokens) * num_kv_heads;
     cudaLaunchConfig_t cfg = {};
@@ -90,12 +92,14 @@ cudaError_t launch_reshape(const void* k, const void* v, void* k_cache, void* v_
     const uint16_t* vv = static_cast<const uint16_t*>(v);
     if (cache_fp8) {
         return src_bf16 ? cudaLaunchKernelEx(&cfg, reshape_kernel<true, true>, kk, vv, k_cache, v_cache, slots,
-                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale, scale_stride)
+                                             num_tokens, num_kv_heads, num_blocks, block_shift, k_scale, v_scale,
+                                             scale_stride)
                         : cudaLaunchKernelEx(&cfg, reshape_kernel<false, true>, kk, vv, k_cache, v_cache, slots,
-                                             num_tokens, num_kv_heads, num_blocks, k_scale, v_scale, scale_stride);
+                                             num_tokens, num_kv_heads, num_blocks, block_shift, k_scale, v_scale,
+                                             scale_stride);
     }
     return cudaLaunchKernelEx(&cfg, reshape_kernel<true, false>, kk, vv, k_cache, v_cache, slots, num_tokens,
-                              num_kv_heads, num_blocks, k_scale, v_scale, scale_stride);
+                              num_kv_heads, num_blocks, block_shift, k_scale, v_scale, scale_stride);
 }
 
 }  // namespace pa

@@ -259,40 +259,46 @@ def poison_value(dtype: str) -> int:
 
 # -- the named workloads ---------------------------------------------------------
 
-def tiny(device, seed: int = 1001) -> Workload:
+def tiny(device, seed: int = 1001, block_size: int = BLOCK_SIZE) -> Workload:
     ctx = [7, 16, 30, 45]
     return build_workload(name="tiny", seed=seed, device=device, num_layers=1,
                           seq_lens=[c + 1 for c in ctx], q_lens=[1] * 4, num_q_heads=8,
-                          num_kv_heads=2, pool_blocks=64)
+                          num_kv_heads=2, pool_blocks=64 * BLOCK_SIZE // block_size, block_size=block_size)
 
 
-def qwen25_15b(device, seed: int = 1002, num_layers: int = 28, batch: int = 64) -> Workload:
+def qwen25_15b(device, seed: int = 1002, num_layers: int = 28, batch: int = 64,
+               block_size: int = BLOCK_SIZE) -> Workload:
     g = torch.Generator(device="cpu").manual_seed(seed)
     lens = torch.randint(512, 4097, (batch,), generator=g).tolist()
     return build_workload(name="qwen2.5-1.5b", seed=seed, device=device, num_layers=num_layers,
-                          seq_lens=lens, q_lens=[1] * batch, num_q_heads=12, num_kv_heads=2)
+                          seq_lens=lens, q_lens=[1] * batch, num_q_heads=12, num_kv_heads=2,
+                          block_size=block_size)
 
 
 def gqa40_8k(device, seed: int = 1003, num_layers: int = 40, batch: int = 40,
-             seq_len: int = 8192) -> Workload:
+             seq_len: int = 8192, block_size: int = BLOCK_SIZE) -> Workload:
     return build_workload(name="gqa40-8k", seed=seed, device=device, num_layers=num_layers,
                           seq_lens=[seq_len] * batch, q_lens=[1] * batch, num_q_heads=32,
-                          num_kv_heads=8, q_dtype="fp16", cache_dtype="fp16", extra_blocks=64)
+                          num_kv_heads=8, q_dtype="fp16", cache_dtype="fp16", extra_blocks=64,
+                          block_size=block_size)
 
 
-def shared_prefix(device, seed: int = 1004, batch: int = 128, prefix_blocks: int = 128,
-                  max_suffix: int = 1000) -> Workload:
+def shared_prefix(device, seed: int = 1004, batch: int = 128, prefix_tokens: int = 2048,
+                  max_suffix: int = 1000, block_size: int = BLOCK_SIZE) -> Workload:
+    # the prefix is prefix_tokens / block_size aliased blocks (128 of 16 tokens by default)
+    assert prefix_tokens % block_size == 0
     g = torch.Generator(device="cpu").manual_seed(seed)
     suffix = torch.randint(0, max_suffix + 1, (batch,), generator=g).tolist()
-    lens = [prefix_blocks * BLOCK_SIZE + x for x in suffix]
+    lens = [prefix_tokens + x for x in suffix]
     return build_workload(name="shared-prefix", seed=seed, device=device, num_layers=1,
                           seq_lens=lens, q_lens=[1] * batch, num_q_heads=32, num_kv_heads=8,
-                          shared_prefix_blocks=prefix_blocks, write_new=False)
+                          shared_prefix_blocks=prefix_tokens // block_size, write_new=False,
+                          block_size=block_size)
 
 
 def mixed_fp8(device, seed: int = 1005, num_decode: int = 16, num_chunks: int = 2,
               chunk_len: int = 512, chunk_ctx: int = 4096, median: int = 8192,
-              sigma: float = 1.0, cap: int = 32768) -> Workload:
+              sigma: float = 1.0, cap: int = 32768, block_size: int = BLOCK_SIZE) -> Workload:
     g = torch.Generator(device="cpu").manual_seed(seed)
     z = torch.randn(num_decode, generator=g, dtype=torch.float64)
     dec = [int(min(cap, max(1, round(math.exp(math.log(median) + sigma * float(x)))))) for x in z]
@@ -300,7 +306,7 @@ def mixed_fp8(device, seed: int = 1005, num_decode: int = 16, num_chunks: int = 
     qls = [1] * num_decode + [chunk_len] * num_chunks
     return build_workload(name="mixed-fp8", seed=seed, device=device, num_layers=1, seq_lens=lens,
                           q_lens=qls, num_q_heads=64, num_kv_heads=8, q_dtype="bf16",
-                          cache_dtype="fp8")
+                          cache_dtype="fp8", block_size=block_size)
 
 
 NAMED = {

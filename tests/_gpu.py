@@ -110,8 +110,12 @@ def compare(gpu_out: torch.Tensor, rows, ref: np.ndarray, what: str = ""):
     rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
     # rounding of the probabilities and of the output is ~2^-9 relative per element; the
     # absolute term 1e-2 * rms (instead of 1e-2) still catches dropped or doubled blocks
-    # when outputs are small, where the stated bound alone would not
-    guard = err <= 1e-2 * np.abs(ref) + 1e-2 * rms
+    # when outputs are small, where the stated bound alone would not.  A row over a few
+    # keys is not an average: its terms p_i V_i keep the size of V, they can cancel, and
+    # the 16-bit rounding of p_i then errs by ~2^-9 of the terms, so the absolute term
+    # takes the larger of the batch rms and the row's own rms
+    row_rms = np.sqrt(np.mean(ref ** 2, axis=-1, keepdims=True)) if ref.size else 0.0
+    guard = err <= 1e-2 * np.abs(ref) + 1e-2 * np.maximum(rms, row_rms)
     assert guard.all(), f"{what}: max err {err.max():.3e} vs rms {rms:.3e}"
     return float(err.max(initial=0.0)), rms
 

@@ -57,7 +57,8 @@ def _decode(lib, **kw):
 
 def test_decode_host_checks(lib):
     assert _decode(lib, d=64) == 2                         # head_dim != 128 unsupported
-    assert _decode(lib, bs=32) == 2                        # block_size != 16 unsupported
+    for bs in (4, 12, 64):
+        assert _decode(lib, bs=bs) == 2                    # block sizes other than 8, 16, 32
     assert _decode(lib, Hq=7) == 1                         # H_q not a multiple of H_kv
     assert _decode(lib, B=-1) == 1
     assert _decode(lib, B=9000) == 1                       # more sequences than supported
@@ -73,6 +74,7 @@ def test_reshape_host_checks(lib):
     f = lib.pa_reshape_and_cache
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 16, 10, 0, 0, None, None, None) == 2
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 16, 10, 0, 1, None, None, None) == 2
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 64, 10, 0, 0, None, None, None) == 2   # block size 64
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 16, 10, 0, 2, None, None, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, None, 4, 2, 128, 16, 10, 0, 0, None, None, None) == 1
     assert f(None, None, None, None, None, 0, 2, 128, 16, 10, 0, 0, None, None, None) == 0   # nothing to do

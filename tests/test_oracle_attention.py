@@ -318,3 +318,80 @@ def test_write_then_decode_poisoned_pool_is_finite_and_dense():
     assert np.all(np.isfinite(got))
     before = oracle_decode(w)
     assert np.all(np.isnan(before))   # without the write, the poisoned new slot is read
+
+
+# -- other block sizes ("Basics of LLM Inference and vLLM Internals", s.11 question 3) ----
+
+def _case_bs(seed, lens, G, bs, cache="bf16", q_lens=None, write_new=False):
+    return W.build_workload(name="t", seed=seed, device="cpu", num_layers=1, seq_lens=lens,
+                            q_lens=q_lens or [1] * len(lens), num_q_heads=G * 2, num_kv_heads=2,
+                            cache_dtype=cache, extra_blocks=8, write_new=write_new, block_size=bs)
+
+
+@pytest.mark.parametrize("bs", [8, 32])
+@pytest.mark.parametrize("cache", ["bf16", "fp8"])
+def test_decode_other_block_sizes_equal_dense(bs, cache):
+    lens = [1, 7, 8, 9, 31, 32, 33, 150]
+    w = _case_bs(40 + bs, lens, 4, bs, cache=cache)
+    assert w.k_cache[0].shape[2] == bs
+    got = oracle_decode(w)
+    kc, vc = workload_values(w)
+    q = values(w.q[0])
+    tables = w.block_tables.numpy()
+    for s, n in enumerate(lens):
+        K, V = dense_kv(kc, vc, tables[s], n, block_size=bs)
+        np.testing.assert_allclose(got[s], sdpa(q[s:s + 1], K, V, w.scale)[0], atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("bs", [8, 32])
+def test_mixed_other_block_sizes_equal_dense_causal(bs):
+    lens, qls = [30, 100, 9, 77], [1, 41, 9, 3]
+    w = _case_bs(50 + bs, lens, 4, bs, q_lens=qls)
+    got = _oracle_mixed(w)
+    kc, vc = workload_values(w)
+    q = values(w.q[0])
+    qsl = w.query_start_loc.tolist()
+    for s, (n, ql) in enumerate(zip(lens, qls)):
+        K, V = dense_kv(kc, vc, w.block_tables[s].numpy(), n, block_size=bs)
+        pos = n - ql + np.arange(ql)
+        mask = np.arange(n)[None, :] <= pos[:, None]
+        ref = sdpa(q[qsl[s]:qsl[s + 1]], K, V, w.scale, mask=mask)
+        np.testing.assert_allclose(got[qsl[s]:qsl[s + 1]], ref, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("bs", [8, 32])
+def test_reshape_other_block_sizes_place_bits(bs):
+    w = _case_bs(60 + bs, [5, 8, 9, 32, 33], 4, bs, write_new=True)
+    kc0, vc0 = raw(w.k_cache[0]), raw(w.v_cache[0])
+    slots = w.slot_mapping.numpy()
+    kc, vc = oracle.reshape_and_cache(raw(w.k_new[0]), raw(w.v_new[0]), oracle.BF16, kc0, vc0, oracle.BF16, slots)
+    exp_k, exp_v = kc0.copy(), vc0.copy()
+    for t, sl in enumerate(slots):
+        exp_k[sl // bs, :, sl % bs, :] = raw(w.k_new[0][t])
+        exp_v[sl // bs, :, sl % bs, :] = raw(w.v_new[0][t])
+    assert np.array_equal(kc, exp_k) and np.array_equal(vc, exp_v)
+
+
+def test_block_size_does_not_change_the_result():
+    # the same tokens stored in blocks of 8, 16 and 32 give the same float64 output
+    lens = [5, 77, 40]
+    base = _case_bs(70, lens, 4, 16)
+    kb, vb = raw(base.k_cache[0]), raw(base.v_cache[0])
+    bt0 = base.block_tables.numpy()
+    outs = []
+    for bs in (8, 16, 32):
+        nb = sum(-(-n // bs) for n in lens)
+        kc = np.zeros((nb, 2, bs, 128), kb.dtype)
+        vc = np.zeros_like(kc)
+        bt = np.full((len(lens), max(-(-n // bs) for n in lens)), -1, np.int32)
+        nxt = 0
+        for s, n in enumerate(lens):
+            for j in range(-(-n // bs)):
+                bt[s, j] = nxt
+                nxt += 1
+            for t in range(n):
+                kc[bt[s, t // bs], :, t % bs] = kb[bt0[s, t // 16], :, t % 16]
+                vc[bt[s, t // bs], :, t % bs] = vb[bt0[s, t // 16], :, t % 16]
+        outs.append(oracle.decode(raw(base.q[0]), oracle.BF16, kc, vc, oracle.BF16, bt,
+                                  np.array(lens, np.int32), base.scale))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[2], outs[1])
