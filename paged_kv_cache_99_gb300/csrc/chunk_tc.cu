@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         q0 = p.query_start_loc[s];
         q_len = p.query_start_loc[s + 1] - q0;
         n = p.seq_lens[s];
-        if (n - q_len < 0 || n > p.max_blocks * p.block_size) {   // inconsistent lengths
+        if (q0 < 0 || q_len < 0 || q0 + q_len > p.total_rows ||    // rows outside q
+            n - q_len < 0 || n > p.max_blocks * p.block_size) {    // inconsistent lengths
             if (threadIdx.x == 0) atomicOr(p.status, kDevErrRange);
             return;
         }

@@ -73,9 +73,12 @@ __device__ __forceinline__ int worker_of(long long f, long long T, int W) {
     return static_cast<int>(((f + 1) * W - 1) / T);
 }
 
-// Decode rows of a mixed batch are the sequences with q_len == 1.
+// Decode rows of a mixed batch are the sequences with q_len == 1 (whose row lies
+// inside q: a malformed query_start_loc is recorded by the prologue and its rows skipped).
 __device__ __forceinline__ bool decode_row(const DecodeParams& p, int s) {
-    return p.query_start_loc == nullptr || p.query_start_loc[s + 1] - p.query_start_loc[s] == 1;
+    if (p.query_start_loc == nullptr) return true;
+    const int a = p.query_start_loc[s];
+    return p.query_start_loc[s + 1] - a == 1 && a >= 0 && a < p.total_rows;
 }
 
 // Blocks sequence s contributes to the flattened order (its blocks x units); a
@@ -173,6 +176,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     }
     // empty decode rows produce zeros; over-long sequences are an input error
     for (int s = blockIdx.x; s < B; s += gridDim.x) {
+        if (mixed && threadIdx.x == 0) {
+            const int a = p.query_start_loc[s], b = p.query_start_loc[s + 1];
+            if (a < 0 || b < a || b > p.total_rows) atomicOr(p.status, kDevErrRange);
+        }
         if (!eligible(s)) continue;
         const int n = p.seq_lens[s];
         if (threadIdx.x == 0 && n > p.max_blocks * p.block_size) atomicOr(p.status, kDevErrRange);

@@ -165,7 +165,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
                       const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads, float scale,
                       pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
                       void* workspace, size_t workspace_bytes, int num_workers, int num_blocks, int block_size,
-                      cudaStream_t stream, bool overlap_prior = false, bool cascade = false,
+                      int total_rows, cudaStream_t stream, bool overlap_prior = false, bool cascade = false,
                       int first_block = 0) {
     int dev = 0;
     DeviceState* st = device_state(&dev);
@@ -222,6 +222,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.ml = reinterpret_cast<float*>(ws + lay.ml_off);
     p.partial = reinterpret_cast<float4*>(ws + lay.partial_off);
     p.num_seqs = num_seqs;
+    p.total_rows = total_rows;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = num_q_heads / num_kv_heads;
@@ -286,6 +287,7 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.scale_stride = scale_stride_of(cache_dtype);
     p.status = static_cast<int*>(workspace);
     p.num_seqs = num_seqs;
+    p.total_rows = total_q;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = group;
@@ -431,7 +433,8 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void
     if (num_seqs == 0) return PA_OK;
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
-                       workspace_bytes, num_workers, num_blocks, block_size, reinterpret_cast<cudaStream_t>(stream));
+                       workspace_bytes, num_workers, num_blocks, block_size, num_seqs,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -481,7 +484,8 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
     }
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
-                       workspace_bytes, workers, num_blocks, block_size, cs, prefix_units > 0, true, prefix_units);
+                       workspace_bytes, workers, num_blocks, block_size, num_seqs, cs, prefix_units > 0, true,
+                       prefix_units);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -525,7 +529,7 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
     // chunk grid leaves idle
     return decode_impl(out, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                        num_seqs, num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale,
-                       workspace, workspace_bytes, 0, num_blocks, block_size, cs, chunks);
+                       workspace, workspace_bytes, 0, num_blocks, block_size, total_q, cs, chunks);
 }
 
 pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -557,7 +561,7 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
     if (s != PA_OK) return s;
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, scratch,
-                       kNoAllocScratchBytes, 0, num_blocks, block_size, cs);
+                       kNoAllocScratchBytes, 0, num_blocks, block_size, num_seqs, cs);
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int num_pairs,

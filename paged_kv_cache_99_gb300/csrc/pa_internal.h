@@ -46,6 +46,7 @@ struct DecodeParams {
     float* ml;                        // [slots][16]: running max (8 heads), sum (8 heads)
     float4* partial;                  // [slots][8][32]: unnormalised output fragments
     int num_seqs;
+    int total_rows;                   // rows of q and out (num_seqs, or total_q of a mixed batch)
     int num_q_heads;
     int num_kv_heads;
     int group;                        // query heads per KV head
@@ -83,6 +84,7 @@ struct ChunkParams {
     int scale_stride;                 // FP8 scales: 0 one per tensor, 1 one per KV head
     int* status;
     int num_seqs;
+    int total_rows;                   // rows of q and out
     int num_q_heads;
     int num_kv_heads;
     int group;

@@ -253,3 +253,26 @@ def test_mixed_zero_length_rows_and_whole_prompt_chunk():
     out, _, _ = gpu_step(w)
     rows, ref = oracle_step(w)
     compare(out, rows, ref, "zero-length + full prompt")
+
+
+@pytest.mark.parametrize("bad", ["chunk_past_end", "decode_row_past_end"])
+def test_mixed_rows_outside_q_are_recorded_not_faulted(bad):
+    # query_start_loc naming rows past total_q: the kernels check every row range
+    # against the size of q before touching it, record the error and skip the row
+    lens, qls = [30, 100, 45], [1, 20, 1]
+    w = _case(51, lens, 4, q_lens=qls, write_new=False)
+    qsl = w.query_start_loc.clone()
+    total_q = int(qsl[-1])
+    if bad == "chunk_past_end":
+        qsl[3] = total_q + 9          # sequence 2 becomes a chunk running 9 rows past the end of q
+    else:
+        qsl[2] = total_q + 3          # sequence 2's decode row is past the end of q (and
+        qsl[3] = total_q + 4          # sequence 1's chunk with it)
+    out = torch.zeros_like(w.q[0])
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads)
+    pa.pa_mixed(out, w.q[0], qsl, w.k_cache[0], w.v_cache[0], w.block_tables, w.seq_lens, 30, w.scale, ws)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_status(ws) == pa.PA_ERR_OUT_OF_RANGE
+    # the well-formed decode row of sequence 0 is still right
+    rows, ref = oracle_step(w, seqs=[0])
+    compare(out, rows, ref, "untouched decode row")
