@@ -555,44 +555,23 @@ constexpr int kBatch = 8;   // slots per round trip of the combine
 // Log-sum-exp combine of the units split across workers:
 //   out = sum_i e^{m_i - M} o_i / sum_i e^{m_i - M} l_i,   M = max_i m_i,
 // where worker i left its unnormalised output o_i, running max m_i (log2 units)
-// and running sum l_i.  One CTA per unit, one warp per 16-wide slice of d; a
-// lane owns heads 2t, 2t+1 of the fragment layout.  Before waiting for the
-// decode grid, the CTA finds its unit's place in the flattened order from the
-// lengths (the decode grid computes the same prefix); after it, one round trip
+// and running sum l_i.  One CTA per unit at a time, one warp per 16-wide slice of
+// d; a lane owns heads 2t, 2t+1 of the fragment layout.  The unit's place in the
+// flattened order comes from `pre` (the block prefix per sequence, which the CTA
+// computed from the lengths before waiting for the decode grid), or for large
+// batches from the plan the decode grid published; after the wait one round trip
 // brings up to kBatch slots' fragments together with their (m, l) for the lane's
 // two heads, reduced in registers (online across batches): no shuffles.
 template <bool OutBf16, bool Fp8Layout>
-__device__ __forceinline__ void combine_unit(const DecodeParams& p, int u) {
+__device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const int* pre_sum) {
     const int UH = p.num_kv_heads * p.head_groups;
     const int s = u / UH, uh = u % UH;
     const int B = p.num_seqs;
     const int dt = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
     long long lo = 0, T = 0;
     if (B <= kCombineScanSeqs) {
-        // the prefix from the lengths, overlapping the decode grid's tail
-        __shared__ long long red[2][8];
-        __syncthreads();          // the previous unit's readers of red are done
-        long long before = 0, total = 0;
-        for (int i = threadIdx.x; i < B; i += blockDim.x) {
-            const int nbl = unit_blocks_of(p, i, UH);
-            total += nbl;
-            if (i < s) before += nbl;
-        }
-#pragma unroll
-        for (int o2 = 16; o2 >= 1; o2 >>= 1) {
-            before += __shfl_xor_sync(0xffffffffu, before, o2);
-            total += __shfl_xor_sync(0xffffffffu, total, o2);
-        }
-        if (lane == 0) {
-            red[0][dt] = before;
-            red[1][dt] = total;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            lo += red[0][k];
-            T += red[1][k];
-        }
+        lo = pre_sum[s];
+        T = pre_sum[B];
     } else {
         grid_dependency_wait();
         lo = p.plan[s];
@@ -698,10 +677,43 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u) {
 
 // Grid-stride over the units: a few CTAs per SM (about 100 registers per thread
 // with 8-slot batches) cover any number of units without waves of one-CTA SMs.
+// For batches of up to kCombineScanSeqs sequences every CTA first builds the
+// exclusive block prefix over the sequences in shared memory, overlapping the
+// decode grid's tail; the units it then visits only look it up.
 template <bool OutBf16, bool Fp8Layout>
 __global__ void __launch_bounds__(256, 2) combine_kernel(const DecodeParams p) {
-    const long long units = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.head_groups;
-    for (long long u = blockIdx.x; u < units; u += gridDim.x) combine_unit<OutBf16, Fp8Layout>(p, static_cast<int>(u));
+    __shared__ int pre_sum[kCombineScanSeqs + 1];
+    __shared__ int warp_sum[8];
+    const int B = p.num_seqs;
+    const int UH = p.num_kv_heads * p.head_groups;
+    if (B <= kCombineScanSeqs) {
+        // thread i sums sequences [per i, per (i + 1)), then a scan over threads
+        const int per = (B + 255) / 256;
+        const int beg = min(B, static_cast<int>(threadIdx.x) * per), end = min(B, beg + per);
+        int own = 0;
+        for (int i = beg; i < end; ++i) own += unit_blocks_of(p, i, UH);
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int inc = own;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o2);
+            if (lane >= o2) inc += y;
+        }
+        if (lane == 31) warp_sum[warp] = inc;
+        __syncthreads();
+        int before = 0;
+        for (int k = 0; k < warp; ++k) before += warp_sum[k];
+        int run = before + inc - own;              // exclusive prefix of this thread's first sequence
+        for (int i = beg; i < end; ++i) {
+            pre_sum[i] = run;
+            run += unit_blocks_of(p, i, UH);
+        }
+        if (threadIdx.x == 255) pre_sum[B] = before + inc;
+        __syncthreads();
+    }
+    const long long units = static_cast<long long>(B) * UH;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x)
+        combine_unit<OutBf16, Fp8Layout>(p, static_cast<int>(u), pre_sum);
 }
 
 // ---------------------------------------------------------------------------

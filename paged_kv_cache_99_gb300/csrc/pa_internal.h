@@ -17,11 +17,11 @@ constexpr int kBlockSize = 16;
 constexpr int kMaxSeqs = 8192;
 constexpr int kDecodeWarps = 4;        // warps per decode CTA
 constexpr int kMaxDecodeCtasPerSm = 2;
-constexpr int kHeadsPerGroup = 8;
+constexpr int kHeadsPerGroup = 8;          // query heads handled by one decode unit (MMA N)
 // Up to this many sequences the combine kernel finds a unit's place in the flattened
 // order itself (before waiting for the decode grid); above it the decode grid
 // publishes its block prefix in the workspace.
-constexpr int kCombineScanSeqs = 1024;      // query heads handled by one decode unit (MMA N)
+constexpr int kCombineScanSeqs = 1024;
 
 // Bits of the device-side status word (first word of the workspace).
 constexpr int kDevErrTimeout = 1;
