@@ -48,6 +48,8 @@ DESCRIPTIONS = {
     "gqa40-8k": "40-layer GQA decode: B=40 at 8192 tokens, H_q=32, H_kv=8, d=128, block 16, fp16 KV",
     "shared-prefix": "shared-prefix decode: 1 layer, B=128, H_q=32, H_kv=8, bf16, 128 aliased prefix blocks "
                      "+ private suffix U[0,1000]",
+    "shared-prefix-long": "shared-prefix decode, long prompt: 1 layer, B=32, H_q=32, H_kv=8, bf16, 512 aliased "
+                          "prefix blocks (8192 tokens) + private suffix U[0,512]",
     "mixed-fp8": "mixed fp8: 1 layer, H_q=64, H_kv=8, e4m3 KV, 16 decode rows (lognormal median 8192, cap 32768) "
                  "+ 2 prefill chunks of 512 on 4096-token contexts",
 }
@@ -63,7 +65,8 @@ def describe(name: str, block_size: int) -> str:
     d = DESCRIPTIONS.get(name, name)
     if block_size != W.BLOCK_SIZE:
         d = d.replace("block 16", f"block {block_size}").replace(
-            "128 aliased prefix blocks", f"2048-token aliased prefix ({2048 // block_size} blocks of {block_size})")
+            "128 aliased prefix blocks", f"2048-token aliased prefix ({2048 // block_size} blocks of {block_size})").replace(
+            "512 aliased prefix blocks", f"{8192 // block_size} aliased prefix blocks of {block_size}")
     return d
 
 
@@ -242,10 +245,11 @@ def run_ours(args, rank, world, local):
     # every replica runs the same workload (weak scaling)
     w = W.make(args.workload, dev, **({"block_size": args.block_size} if args.block_size != W.BLOCK_SIZE else {}))
     layers_caches = [(w.k_cache[l], w.v_cache[l]) for l in range(w.num_layers)]
-    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, device=dev)
+    cascade = bool(args.cascade)
+    # the cascade gets the workspace that lets it cut the prefix into key segments
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, device=dev, shared_prefix=cascade)
     outs = [torch.empty_like(w.q[l]) for l in range(w.num_layers)]
     kv_bytes = kv_read_bytes(w)
-    cascade = bool(args.cascade)
     if cascade and not (w.is_decode_only and w.shared_prefix_blocks > 0):
         raise SystemExit("--cascade needs a decode workload whose tables share leading blocks (shared-prefix)")
     step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, cascade=cascade))

@@ -131,6 +131,14 @@ PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cach
  */
 PA_API size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
 
+/*
+ * Bytes of workspace with which pa_decode_shared_prefix can cut the shared
+ * prefix into as many key segments as it wants (up to 16 partials per query
+ * row: num_seqs * num_q_heads * 520 bytes each beyond pa_workspace_size).
+ * Same rules as pa_workspace_size.  Returns 0 for invalid arguments.
+ */
+PA_API size_t pa_workspace_size_shared_prefix(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
+
 /* Default number of decode workers (warps) on the current device. */
 PA_API int pa_default_workers(void);
 
@@ -199,15 +207,21 @@ PA_API pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, con
  *
  * The prefix keys are read once for the whole batch: every decode row of every
  * sequence is contracted against them on the tensor cores as one dense tile
- * grid (one CTA per 256 query rows of a KV head), leaving an unnormalised
- * partial per row; the private blocks after the prefix stream through the
- * decode kernel, launched behind it and running beside it; the combine kernel
- * merges both by log-sum-exp.  prefix_blocks == 0 reduces to pa_decode with
- * every row merged by the combine.
+ * grid (one CTA per 256 query rows of a KV head and key segment), leaving an
+ * unnormalised partial per row and segment; the private blocks after the
+ * prefix stream through the decode kernel; the combine kernel merges all of
+ * them by log-sum-exp.  The prefix is cut into key segments of whole 128-key
+ * steps until its grid has about one CTA per SM, as far as the workspace
+ * holds the extra partials; a prefix grid under half the SMs runs beside the
+ * decode grid (which then takes the other SMs), a larger one runs first.
+ * prefix_blocks == 0 reduces to pa_decode with every row merged by the
+ * combine.
  *
  *   prefix_blocks  host, 0 <= prefix_blocks <= max_blocks_per_seq
  *   workspace      at least pa_workspace_size(num_seqs, num_q_heads,
- *                  num_kv_heads, head_dim) bytes
+ *                  num_kv_heads, head_dim) bytes (then the prefix is one
+ *                  segment); pa_workspace_size_shared_prefix bytes allow
+ *                  every split
  * Other arguments as pa_decode; results agree with pa_decode to rounding.
  */
 PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,

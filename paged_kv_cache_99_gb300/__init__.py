@@ -59,6 +59,8 @@ def _lib():
     lib.pa_reshape_and_cache.restype = I
     lib.pa_workspace_size.argtypes = [I, I, I, I]
     lib.pa_workspace_size.restype = Z
+    lib.pa_workspace_size_shared_prefix.argtypes = [I, I, I, I]
+    lib.pa_workspace_size_shared_prefix.restype = Z
     lib.pa_default_workers.argtypes = []
     lib.pa_default_workers.restype = I
     lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
@@ -149,9 +151,16 @@ def pa_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_d
     return int(_lib().pa_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim))
 
 
-def new_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, device=None) -> torch.Tensor:
-    """Workspace of pa_workspace_size bytes (zeroed, so the status word starts clear)."""
-    n = pa_workspace_size(num_seqs, num_q_heads, num_kv_heads)
+def pa_workspace_size_shared_prefix(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128) -> int:
+    return int(_lib().pa_workspace_size_shared_prefix(num_seqs, num_q_heads, num_kv_heads, head_dim))
+
+
+def new_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, device=None,
+                  shared_prefix: bool = False) -> torch.Tensor:
+    """Workspace of pa_workspace_size bytes (zeroed, so the status word starts clear);
+    with shared_prefix, pa_workspace_size_shared_prefix bytes (every prefix split)."""
+    size = pa_workspace_size_shared_prefix if shared_prefix else pa_workspace_size
+    n = size(num_seqs, num_q_heads, num_kv_heads)
     if n == 0:
         raise ValueError("invalid workspace arguments")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")

@@ -232,8 +232,15 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     const int jl0 = min(q_len, jf0 + QT) - 1;
     const int jl1 = has_b ? min(q_len, jf1 + QT) - 1 : jl0;
     const int pos_last_cta = qpos(jl1);
-    const int nsteps = pos_last_cta / kTcKeys + 1;
-    const int nsteps_a = qpos(jl0) / kTcKeys + 1;
+    // steps of 128 keys this CTA covers: all up to its last position, or in prefix
+    // mode the key segment blockIdx.z of prefix_steps steps (its own partial)
+    int step0 = 0;
+    int nsteps = pos_last_cta / kTcKeys + 1;
+    int nsteps_a = qpos(jl0) / kTcKeys + 1;
+    if (prefix && p.prefix_steps > 0) {
+        step0 = static_cast<int>(blockIdx.z) * p.prefix_steps;
+        nsteps = nsteps_a = max(min(nsteps - step0, p.prefix_steps), 0);
+    }
     const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
     auto tile_steps = [&](int x) -> int { return x == 0 ? nsteps_a : (has_b ? nsteps : 0); };
 
@@ -258,7 +265,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             const int per_step = kTcKeys >> rsh;                  // pieces per step: 8 or 16
             const int npieces = (pos_last_cta >> rsh) + 1;        // pieces up to the CTA's last key
             auto entry = [&](int i) -> int {
-                const int c = i * per_step + lane;
+                const int c = (step0 + i) * per_step + lane;
                 int y = 0;
                 if (lane < per_step && c < npieces) {
                     const int key = c << rsh;
@@ -284,7 +291,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 const int st = i % kTcStages;
                 const uint32_t par = ((i / kTcStages) - 1) & 1;
                 const int y_next = i + 1 < nsteps ? entry(i + 1) : 0;
-                const int nb = min(per_step, npieces - i * per_step);
+                const int nb = min(per_step, npieces - (step0 + i) * per_step);
                 if (i >= kTcStages && !warp_wait(bar(kBarKEmpty + st), par, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 break;
             }
             tc_fence_after();
-            const int key0 = i * kTcKeys;
+            const int key0 = (step0 + i) * kTcKeys;
             const bool need_mask = key0 + kTcKeys - 1 > pos_first;
             const int lim = pos - key0;                 // columns > lim are masked
             // the whole row of S in registers: one tensor-memory round trip per step
@@ -529,7 +536,11 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             if (ok && prefix && warp_wait(bar(kBarPvDone + x), 0, p.timeout_ns)) {
                 // unnormalised rows and (max, sum) for the combine of the cascade decode
                 tc_fence_after();
-                float4* dst = reinterpret_cast<float4*>(p.prefix_o + qrow);
+                // segment z of the prefix keys: its own rows of partials
+                const size_t seg_rows = static_cast<size_t>(blockIdx.z) * p.num_seqs * p.num_q_heads;
+                float* seg_o = blockIdx.z == 0 ? p.prefix_o : p.prefix_o_extra + (seg_rows - static_cast<size_t>(p.num_seqs) * p.num_q_heads) * kHeadDim;
+                float* seg_ml = blockIdx.z == 0 ? p.prefix_ml : p.prefix_ml_extra + (seg_rows - static_cast<size_t>(p.num_seqs) * p.num_q_heads) * 2;
+                float4* dst = reinterpret_cast<float4*>(seg_o + qrow);
 #pragma unroll 1
                 for (int c = 0; c < kHeadDim / 32; ++c) {
                     uint32_t ov[32];
@@ -543,8 +554,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     }
                 }
                 if (live) {
-                    p.prefix_ml[(qrow / kHeadDim) * 2] = m_used;
-                    p.prefix_ml[(qrow / kHeadDim) * 2 + 1] = l;
+                    seg_ml[(qrow / kHeadDim) * 2] = m_used;
+                    seg_ml[(qrow / kHeadDim) * 2 + 1] = l;
                 }
             } else if (ok && !prefix && warp_wait(bar(kBarPvDone + x), 0, p.timeout_ns)) {
                 tc_fence_after();
@@ -578,7 +589,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         // V(i) 0, V(i) 1, K(i+1) 0, ...
         const int krow = warp == 0 ? lane : 32 + lane;     // key within the item
         auto load_item = [&](const uint8_t* cache, int i, int u, uint4 (&x8)[8]) {
-            const int key = i * kTcKeys + 64 * u + krow;
+            const int key = (step0 + i) * kTcKeys + 64 * u + krow;
             if (i < nsteps && key <= pos_last_cta) {      // later keys get P = 0: store zeros
                 int phys = __ldg(bt + (key >> p.block_shift));
                 if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
@@ -696,7 +707,7 @@ cudaError_t chunk_prepare(CacheKind kind, bool q_bf16, size_t max_smem) {
 cudaError_t launch_chunk(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          const ChunkParams& p, int grid_x, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_x, p.num_kv_heads);
+    cfg.gridDim = dim3(grid_x, p.num_kv_heads, p.prefix_keys > 0 && p.prefix_splits > 1 ? p.prefix_splits : 1);
     cfg.blockDim = dim3(kind == kKindFp8 ? TcCfg<kKindFp8>::kWarps * 32 : TcCfg<kKindBf16>::kWarps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

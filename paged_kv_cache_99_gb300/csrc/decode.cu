@@ -562,7 +562,7 @@ constexpr int kBatch = 8;   // slots per round trip of the combine
 // batches from the plan the decode grid published; after the wait one round trip
 // brings up to kBatch slots' fragments together with their (m, l) for the lane's
 // two heads, reduced in registers (online across batches): no shuffles.
-template <bool OutBf16, bool Fp8Layout>
+template <bool OutBf16, bool Fp8Layout, bool Cascade>
 __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const int* pre_sum) {
     const int UH = p.num_kv_heads * p.head_groups;
     const int s = u / UH, uh = u % UH;
@@ -579,13 +579,13 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
     }
     const int nb = unit_blocks_of(p, s, UH) / UH;
     const int W = static_cast<int>(min(static_cast<long long>(p.num_workers), T));
-    const bool pre = p.cascade && p.first_block > 0;   // every row has a shared-prefix partial
+    const bool pre = Cascade && p.first_block > 0;     // every row has a shared-prefix partial
     int wa = 0, nseg = 0;
     if (nb > 0 && W > 0) {
         const long long fu = lo + static_cast<long long>(uh) * nb;
         wa = worker_of(fu, T, W);
         const int wb = worker_of(fu + nb - 1, T, W);
-        if (wa == wb && !p.cascade) return;   // its only worker wrote the output
+        if (wa == wb && !Cascade) return;     // its only worker wrote the output
         nseg = wb - wa + 1;
     } else if (!pre) {
         return;   // an empty row: the decode grid wrote its zeros
@@ -597,33 +597,9 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
     if (B <= kCombineScanSeqs) grid_dependency_wait();
     float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (pre) {
-        // start from the shared-prefix partial of the lane's two heads, in the
-        // fragment layout of the decode partials
-        const int dA = Fp8Layout ? 16 * dt + 2 * g : 16 * dt + g;
-        const int dB = Fp8Layout ? dA + 1 : dA + 8;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int gh = hg * kHeadsPerGroup + 2 * t + e;
-            if (gh >= p.group) continue;
-            const size_t ri = static_cast<size_t>(row) * p.num_q_heads + h * p.group + gh;
-            const float m = __ldcg(p.prefix_ml + 2 * ri), lsum = __ldcg(p.prefix_ml + 2 * ri + 1);
-            if (e == 0) { M0 = m; L0 = lsum; } else { M1 = m; L1 = lsum; }
-            acc[e] = __ldcg(p.prefix_o + ri * kHeadDim + dA);
-            acc[2 + e] = __ldcg(p.prefix_o + ri * kHeadDim + dB);
-        }
-    }
-    for (int base = 0; base < nseg; base += kBatch) {
-        float4 v[kBatch];
-        float2 mv[kBatch], lv[kBatch];
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int sl = wa + min(base + k, nseg - 1) + u;
-            v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
-            mv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 2 * t));
-            lv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 8 + 2 * t));
-        }
-        const int n = min(kBatch, nseg - base);
+    // fold a batch of n pieces, each (fragment, max, sum) of the lane's two heads,
+    // into the running (M, L, acc) (padding heads may turn to NaN: never written)
+    auto fold = [&](const float4 (&v)[kBatch], const float2 (&mv)[kBatch], const float2 (&lv)[kBatch], int n) {
         float b0 = M0, b1 = M1;
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
@@ -654,6 +630,54 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
                 L1 += lv[k].y * w1;
             }
         }
+    };
+    // the shared-prefix partials of the unit's rows, one per key segment of the
+    // prefix, stored row-wise; fragment element (d, head 2t + e) of the lane is
+    // d = dA (components 0, 1) and dB (2, 3)
+    const int npre = pre ? p.prefix_splits : 0;
+    if (Cascade && npre > 0) {
+        const int dA = Fp8Layout ? 16 * dt + 2 * g : 16 * dt + g;
+        const int dB = Fp8Layout ? dA + 1 : dA + 8;
+        const size_t rows = static_cast<size_t>(B) * p.num_q_heads;
+        for (int base = 0; base < npre; base += kBatch) {
+            float4 v[kBatch];
+            float2 mv[kBatch], lv[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int idx = min(base + k, npre - 1);
+                const float* so = idx == 0 ? p.prefix_o : p.prefix_o_extra + (idx - 1) * rows * kHeadDim;
+                const float* sm = idx == 0 ? p.prefix_ml : p.prefix_ml_extra + (idx - 1) * rows * 2;
+                float o4[4] = {0.f, 0.f, 0.f, 0.f}, m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int gh = hg * kHeadsPerGroup + 2 * t + e;
+                    if (gh >= p.group) continue;
+                    const size_t ri = static_cast<size_t>(row) * p.num_q_heads + h * p.group + gh;
+                    const float2 ml2 = __ldcg(reinterpret_cast<const float2*>(sm + 2 * ri));
+                    m2[e] = ml2.x;
+                    l2[e] = ml2.y;
+                    o4[e] = __ldcg(so + ri * kHeadDim + dA);
+                    o4[2 + e] = __ldcg(so + ri * kHeadDim + dB);
+                }
+                v[k] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                mv[k] = make_float2(m2[0], m2[1]);
+                lv[k] = make_float2(l2[0], l2[1]);
+            }
+            fold(v, mv, lv, min(kBatch, npre - base));
+        }
+    }
+    // the decode slots of the unit's segments
+    for (int base = 0; base < nseg; base += kBatch) {
+        float4 v[kBatch];
+        float2 mv[kBatch], lv[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int sl = wa + min(base + k, nseg - 1) + u;
+            v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
+            mv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 2 * t));
+            lv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 8 + 2 * t));
+        }
+        fold(v, mv, lv, min(kBatch, nseg - base));
     }
     const float vscale = Fp8Layout ? __ldg(p.v_scale + h * p.scale_stride) : 1.0f;
 #pragma unroll
@@ -675,13 +699,14 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
     }
 }
 
-// Grid-stride over the units: a few CTAs per SM (about 100 registers per thread
-// with 8-slot batches) cover any number of units without waves of one-CTA SMs.
-// For batches of up to kCombineScanSeqs sequences every CTA first builds the
+// Grid-stride over the units: a few CTAs per SM cover any number of units without
+// waves of one-CTA SMs.  At most 112 registers per thread, so that a combine CTA
+// fits beside two decode CTAs (136 registers x 128 threads each) and is resident,
+// past its prologue, while the decode grid drains.  For batches of up to kCombineScanSeqs sequences every CTA first builds the
 // exclusive block prefix over the sequences in shared memory, overlapping the
 // decode grid's tail; the units it then visits only look it up.
-template <bool OutBf16, bool Fp8Layout>
-__global__ void __launch_bounds__(256, 2) combine_kernel(const DecodeParams p) {
+template <bool OutBf16, bool Fp8Layout, bool Cascade>
+__global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
     __shared__ int pre_sum[kCombineScanSeqs + 1];
     __shared__ int warp_sum[8];
     const int B = p.num_seqs;
@@ -713,7 +738,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const DecodeParams p) {
     }
     const long long units = static_cast<long long>(B) * UH;
     for (long long u = blockIdx.x; u < units; u += gridDim.x)
-        combine_unit<OutBf16, Fp8Layout>(p, static_cast<int>(u), pre_sum);
+        combine_unit<OutBf16, Fp8Layout, Cascade>(p, static_cast<int>(u), pre_sum);
 }
 
 // ---------------------------------------------------------------------------
@@ -802,11 +827,18 @@ cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.cascade) {
+        if (fp8_cache)
+            return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, true, true>, p)
+                            : cudaLaunchKernelEx(&cfg, combine_kernel<false, true, true>, p);
+        return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, false, true>, p)
+                        : cudaLaunchKernelEx(&cfg, combine_kernel<false, false, true>, p);
+    }
     if (fp8_cache)
-        return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, true>, p)
-                        : cudaLaunchKernelEx(&cfg, combine_kernel<false, true>, p);
-    return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, false>, p)
-                    : cudaLaunchKernelEx(&cfg, combine_kernel<false, false>, p);
+        return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, true, false>, p)
+                        : cudaLaunchKernelEx(&cfg, combine_kernel<false, true, false>, p);
+    return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, false, false>, p)
+                    : cudaLaunchKernelEx(&cfg, combine_kernel<false, false, false>, p);
 }
 
 }  // namespace pa

@@ -166,7 +166,8 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
                       pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
                       void* workspace, size_t workspace_bytes, int num_workers, int num_blocks, int block_size,
                       int total_rows, cudaStream_t stream, bool overlap_prior = false, bool cascade = false,
-                      int first_block = 0) {
+                      int first_block = 0, int prefix_splits = 1, const float* prefix_o_extra = nullptr,
+                      const float* prefix_ml_extra = nullptr) {
     int dev = 0;
     DeviceState* st = device_state(&dev);
     if (!st) return PA_ERR_CUDA;
@@ -237,6 +238,9 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.first_block = cascade ? first_block : 0;
     p.prefix_o = reinterpret_cast<const float*>(ws + lay.prefix_o_off);
     p.prefix_ml = reinterpret_cast<const float*>(ws + lay.prefix_ml_off);
+    p.prefix_splits = prefix_splits;
+    p.prefix_o_extra = prefix_o_extra;
+    p.prefix_ml_extra = prefix_ml_extra;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
@@ -251,7 +255,9 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
                      const int32_t* seq_lens, int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
                      int num_blocks, int block_size, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
                      const float* k_scale, const float* v_scale, void* workspace, cudaStream_t stream,
-                     int prefix_units = 0, float* prefix_o = nullptr, float* prefix_ml = nullptr) {
+                     int prefix_units = 0, float* prefix_o = nullptr, float* prefix_ml = nullptr,
+                     int prefix_splits = 1, int prefix_steps = 0, float* prefix_o_extra = nullptr,
+                     float* prefix_ml_extra = nullptr) {
     DeviceState* st = device_state(nullptr);
     if (!st) return PA_ERR_CUDA;
     const CacheKind kind = kind_of(cache_dtype);
@@ -299,6 +305,10 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.prefix_keys = prefix_units * kBlockSize;
     p.prefix_o = prefix_o;
     p.prefix_ml = prefix_ml;
+    p.prefix_splits = prefix_splits;
+    p.prefix_steps = prefix_steps;
+    p.prefix_o_extra = prefix_o_extra;
+    p.prefix_ml_extra = prefix_ml_extra;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     return cuda_status(launch_chunk(kind, q_bf16, kmap, vmap, p, static_cast<int>(grid_x), smem, stream),
@@ -323,6 +333,20 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
     l.partial_off = l.ml_off + round_up(slots * 16 * 4, 256);
     l.total = l.partial_off + slots * 8 * 32 * sizeof(float4);
     return l;
+}
+
+// Extra prefix segments of a split shared prefix, after the base workspace:
+// [splits - 1][rows][128] f32 partial rows, then [splits - 1][rows][2] (max, sum).
+struct PrefixExtra {
+    size_t o_off, ml_off, end;
+};
+
+PrefixExtra prefix_extra_layout(size_t base, size_t rows, int splits) {
+    PrefixExtra e;
+    e.o_off = round_up(base, 256);
+    e.ml_off = round_up(e.o_off + static_cast<size_t>(splits - 1) * rows * kHeadDim * sizeof(float), 256);
+    e.end = e.ml_off + static_cast<size_t>(splits - 1) * rows * 2 * sizeof(float);
+    return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -415,6 +439,12 @@ size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int he
         .total;
 }
 
+size_t pa_workspace_size_shared_prefix(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+    const size_t base = pa_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim);
+    if (base == 0) return 0;
+    return prefix_extra_layout(base, static_cast<size_t>(num_seqs) * num_q_heads, kMaxPrefixSplits).end;
+}
+
 int pa_default_workers(void) {
     DeviceState* st = device_state(nullptr);
     return st ? max_workers(*st) : 0;
@@ -451,9 +481,42 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
     if (num_seqs == 0) return PA_OK;
     if (workspace_bytes < pa_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)) return PA_ERR_WORKSPACE;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    DeviceState* st = device_state(nullptr);
+    if (!st) return PA_ERR_CUDA;
     // the split runs at a 16-key boundary: with 8-token blocks an odd last shared
     // block goes to every sequence's own part
     const int prefix_units = static_cast<int>(static_cast<long long>(prefix_blocks) * block_size / kBlockSize);
+    const size_t base = pa_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim);
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int splits = 1, steps = 0;
+    long long pair_ctas = 0;
+    if (prefix_units > 0) {
+        // Key segments of the prefix (each leaves its own partial rows): only when the
+        // prefix grid, 4 us or so per 128-key step of a CTA, would outlast the decode
+        // of the private blocks (bounded from the table width at 5 TB/s), and only as
+        // many as keep the prefix grid on under half the SMs and fit the workspace.
+        const int per_cta = (chunk_rows() / (num_q_heads / num_kv_heads)) * chunk_tiles_per_cta();
+        pair_ctas = static_cast<long long>((num_seqs + per_cta - 1) / per_cta) * num_kv_heads;
+        const int total_steps = (prefix_units * kBlockSize + 127) / 128;
+        const long long suffix_tokens =
+            static_cast<long long>(max_blocks_per_seq) * block_size - static_cast<long long>(prefix_units) * kBlockSize;
+        const double suffix_bytes = static_cast<double>(num_seqs) * num_kv_heads * (suffix_tokens > 0 ? suffix_tokens : 0) *
+                                    kHeadDim * 2 * (is_fp8(cache_dtype) ? 1 : 2);
+        const double decode_us = suffix_bytes / 5.0e6;
+        long long cap = (st->sms / 2) / pair_ctas;
+        if (cap > total_steps) cap = total_steps;
+        if (cap > kMaxPrefixSplits) cap = kMaxPrefixSplits;
+        auto prefix_us = [&](int k) { return 4.0 * ((total_steps + k - 1) / k) + 6.0; };
+        while (splits < cap && prefix_us(splits) > decode_us &&
+               prefix_extra_layout(base, rows, splits + 1).end <= workspace_bytes)
+            ++splits;
+        steps = (total_steps + splits - 1) / splits;
+        splits = (total_steps + steps - 1) / steps;     // every segment has at least one step
+    }
+    const PrefixExtra ex = prefix_extra_layout(base, rows, splits);
+    float* o_extra = splits > 1 ? reinterpret_cast<float*>(ws + ex.o_off) : nullptr;
+    float* ml_extra = splits > 1 ? reinterpret_cast<float*>(ws + ex.ml_off) : nullptr;
     if (prefix_units > 0) {
         // the shared prefix once, as a dense contraction of every decode row against its keys
         const CacheKind kind = kind_of(cache_dtype);
@@ -464,28 +527,22 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
         if (s != PA_OK) return s;
         const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads,
                                                             head_groups_of(num_q_heads, num_kv_heads), 0);
-        uint8_t* ws = static_cast<uint8_t*>(workspace);
         s = chunk_impl(out, q, nullptr, k_cache, v_cache, kmap, vmap, block_tables, max_blocks_per_seq, seq_lens,
                        num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, block_size, scale, q_dtype,
                        cache_dtype, k_scale, v_scale, workspace, cs, prefix_units,
-                       reinterpret_cast<float*>(ws + lay.prefix_o_off), reinterpret_cast<float*>(ws + lay.prefix_ml_off));
+                       reinterpret_cast<float*>(ws + lay.prefix_o_off), reinterpret_cast<float*>(ws + lay.prefix_ml_off),
+                       splits, splits > 1 ? steps : 0, o_extra, ml_extra);
         if (s != PA_OK) return s;
     }
-    // the private suffixes stream beside it, on the SMs the prefix grid leaves free;
+    // the private suffixes stream beside the prefix grid, on the SMs it leaves free;
     // the combine merges both
     int workers = 0;
-    if (prefix_units > 0) {
-        DeviceState* st = device_state(nullptr);
-        if (!st) return PA_ERR_CUDA;
-        const int per_cta = (chunk_rows() / (num_q_heads / num_kv_heads)) * chunk_tiles_per_cta();
-        const long long prefix_ctas = static_cast<long long>((num_seqs + per_cta - 1) / per_cta) * num_kv_heads;
-        if (prefix_ctas < st->sms / 2)
-            workers = static_cast<int>(static_cast<long long>(max_workers(*st)) * (st->sms - prefix_ctas) / st->sms);
-    }
+    if (prefix_units > 0 && pair_ctas * splits < st->sms / 2)
+        workers = static_cast<int>(static_cast<long long>(max_workers(*st)) * (st->sms - pair_ctas * splits) / st->sms);
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
                        workspace_bytes, workers, num_blocks, block_size, num_seqs, cs, prefix_units > 0, true,
-                       prefix_units);
+                       prefix_units, splits, o_extra, ml_extra);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -22,6 +22,9 @@ constexpr int kHeadsPerGroup = 8;          // query heads handled by one decode 
 // order itself (before waiting for the decode grid); above it the decode grid
 // publishes its block prefix in the workspace.
 constexpr int kCombineScanSeqs = 1024;
+// Most key segments a shared prefix is cut into (pa_workspace_size_shared_prefix
+// holds this many partials per row).
+constexpr int kMaxPrefixSplits = 16;
 
 // Bits of the device-side status word (first word of the workspace).
 constexpr int kDevErrTimeout = 1;
@@ -66,6 +69,9 @@ struct DecodeParams {
     int first_block;                  // shared leading 16-key units (cascade mode)
     const float* prefix_o;            // [num_seqs][num_q_heads][128]: unnormalised prefix output
     const float* prefix_ml;           // [num_seqs][num_q_heads][2]: its (max in log2 units, sum)
+    int prefix_splits;                // prefix partials per row (key segments of the prefix)
+    const float* prefix_o_extra;      // [prefix_splits - 1][num_seqs][num_q_heads][128]
+    const float* prefix_ml_extra;     // [prefix_splits - 1][num_seqs][num_q_heads][2]
     float scale_log2;                 // softmax scale * log2(e)
     unsigned long long timeout_ns;    // bound of every barrier wait
 };
@@ -97,9 +103,17 @@ struct ChunkParams {
     // sequences ([num_seqs][num_q_heads][128]), every one at position prefix_keys - 1,
     // the keys are the first prefix_keys tokens of sequence 0's table, and the
     // output is unnormalised: prefix_o (f32 rows) and prefix_ml (max, sum).
+    // Split prefix: gridDim.z = prefix_splits CTAs per tile pair, segment z covering
+    // steps [z prefix_steps, (z + 1) prefix_steps) of 128 keys; segment 0 writes
+    // prefix_o / prefix_ml, segment z > 0 the (z - 1)-th block of prefix_o_extra /
+    // prefix_ml_extra (same row layout).
     int prefix_keys;
+    int prefix_splits;
+    int prefix_steps;
     float* prefix_o;
     float* prefix_ml;
+    float* prefix_o_extra;
+    float* prefix_ml_extra;
     float scale_log2;
     unsigned long long timeout_ns;
 };

@@ -296,6 +296,13 @@ def shared_prefix(device, seed: int = 1004, batch: int = 128, prefix_tokens: int
                           block_size=block_size)
 
 
+def shared_prefix_long(device, seed: int = 1006, batch: int = 32, prefix_tokens: int = 8192,
+                       max_suffix: int = 512, block_size: int = BLOCK_SIZE) -> Workload:
+    # the other regime of a shared prefix: few sequences behind a long common prompt
+    return shared_prefix(device, seed=seed, batch=batch, prefix_tokens=prefix_tokens, max_suffix=max_suffix,
+                         block_size=block_size)
+
+
 def mixed_fp8(device, seed: int = 1005, num_decode: int = 16, num_chunks: int = 2,
               chunk_len: int = 512, chunk_ctx: int = 4096, median: int = 8192,
               sigma: float = 1.0, cap: int = 32768, block_size: int = BLOCK_SIZE) -> Workload:
@@ -314,6 +321,7 @@ NAMED = {
     "qwen2.5-1.5b": qwen25_15b,
     "gqa40-8k": gqa40_8k,
     "shared-prefix": shared_prefix,
+    "shared-prefix-long": shared_prefix_long,
     "mixed-fp8": mixed_fp8,
 }
 

@@ -123,3 +123,60 @@ def test_cascade_full_size_shared_prefix_sampled():
     pick = sorted({0, 1, int(lens.argmax()), int(lens.argmin()), 77, w.num_seqs - 1})
     rows, ref = oracle_step(w, 0, pick)
     compare(out, rows, ref, "shared-prefix config, sampled rows")
+
+
+# ---- the prefix cut into key segments (workspace with room for the extra partials) ----
+
+def _split_ws(w):
+    return pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, shared_prefix=True)
+
+
+@pytest.mark.parametrize("cache,qd", [("bf16", "bf16"), ("fp16", "fp16"), ("fp8", "bf16")])
+@pytest.mark.parametrize("G", [1, 4, 8, 12])
+@pytest.mark.parametrize("prefix", [24, 37, 130])
+def test_cascade_split_prefix_matches_oracle(cache, qd, G, prefix):
+    # 384, 592 and 2080 prefix keys: 3, 5 and 17 steps of 128 keys, the last two
+    # ending inside a step; 17 steps over at most 16 segments gives segments of 2
+    w = _case(90 + G + prefix, prefix, SUFFIXES, G, cache=cache, qd=qd)
+    out, st = _cascade(w, prefix, ws=_split_ws(w))
+    assert st == pa.PA_OK, pa.pa_status_string(st)
+    rows, ref = oracle_step(w)
+    compare(out, rows, ref, f"split cascade {cache} G={G} prefix={prefix}")
+
+
+def test_cascade_split_limited_by_workspace():
+    # room for two extra partials per row only: three segments
+    w = _case(95, 64, SUFFIXES, 4)
+    base = pa.pa_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads)
+    rows = w.num_seqs * w.num_q_heads
+    extra = 2 * rows * 128 * 4 + 256 + 2 * rows * 2 * 4 + 256
+    ws = torch.zeros(base + extra, dtype=torch.uint8, device=DEV)
+    out, st = _cascade(w, 64, ws=ws)
+    assert st == pa.PA_OK
+    rows_, ref = oracle_step(w)
+    compare(out, rows_, ref, "split limited by workspace")
+
+
+@pytest.mark.parametrize("bs,prefix", [(8, 75), (32, 20)])
+def test_cascade_split_other_block_sizes(bs, prefix):
+    lens = [prefix * bs + x for x in SUFFIXES]
+    w = W.build_workload(name="cascade", seed=96 + bs, device=DEV, num_layers=1, seq_lens=lens,
+                         q_lens=[1] * len(lens), num_q_heads=16, num_kv_heads=2, block_size=bs,
+                         shared_prefix_blocks=prefix, write_new=False)
+    out, st = _cascade(w, prefix, ws=_split_ws(w))
+    assert st == pa.PA_OK
+    rows, ref = oracle_step(w)
+    compare(out, rows, ref, f"split cascade bs={bs}")
+
+
+def test_cascade_split_long_prefix_sampled():
+    # 32 sequences behind an 8192-token prompt: 8 tile-pair CTAs, the prefix cut into
+    # segments until the prefix grid covers half the GPU
+    w = W.make("shared-prefix-long", DEV)
+    out, st = _cascade(w, w.shared_prefix_blocks, ws=_split_ws(w))
+    assert st == pa.PA_OK
+    assert torch.isfinite(out.float()).all()
+    lens = w.seq_lens.cpu().numpy()
+    pick = sorted({0, 1, int(lens.argmax()), int(lens.argmin()), w.num_seqs // 2, w.num_seqs - 1})
+    rows, ref = oracle_step(w, 0, pick)
+    compare(out, rows, ref, "long shared prefix, split, sampled rows")
