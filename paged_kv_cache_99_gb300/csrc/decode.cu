@@ -29,6 +29,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -550,7 +552,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
     if (p.overlap_prior && blockIdx.x == gridDim.x - 1) grid_dependency_wait();
 }
 
-constexpr int kBatch = 8;   // slots per round trip of the combine
 
 // Log-sum-exp combine of the units split across workers:
 //   out = sum_i e^{m_i - M} o_i / sum_i e^{m_i - M} l_i,   M = max_i m_i,
@@ -562,7 +563,7 @@ constexpr int kBatch = 8;   // slots per round trip of the combine
 // batches from the plan the decode grid published; after the wait one round trip
 // brings up to kBatch slots' fragments together with their (m, l) for the lane's
 // two heads, reduced in registers (online across batches): no shuffles.
-template <bool OutBf16, bool Fp8Layout, bool Cascade>
+template <bool OutBf16, bool Fp8Layout, bool Cascade, int kBatch>
 __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const int* pre_sum) {
     const int UH = p.num_kv_heads * p.head_groups;
     const int s = u / UH, uh = u % UH;
@@ -705,7 +706,7 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
 // past its prologue, while the decode grid drains.  For batches of up to kCombineScanSeqs sequences every CTA first builds the
 // exclusive block prefix over the sequences in shared memory, overlapping the
 // decode grid's tail; the units it then visits only look it up.
-template <bool OutBf16, bool Fp8Layout, bool Cascade>
+template <bool OutBf16, bool Fp8Layout, bool Cascade, int kBatch>
 __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
     __shared__ int pre_sum[kCombineScanSeqs + 1];
     __shared__ int warp_sum[8];
@@ -738,7 +739,7 @@ __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
     }
     const long long units = static_cast<long long>(B) * UH;
     for (long long u = blockIdx.x; u < units; u += gridDim.x)
-        combine_unit<OutBf16, Fp8Layout, Cascade>(p, static_cast<int>(u), pre_sum);
+        combine_unit<OutBf16, Fp8Layout, Cascade, kBatch>(p, static_cast<int>(u), pre_sum);
 }
 
 // ---------------------------------------------------------------------------
@@ -827,18 +828,22 @@ cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.cascade) {
-        if (fp8_cache)
-            return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, true, true>, p)
-                            : cudaLaunchKernelEx(&cfg, combine_kernel<false, true, true>, p);
-        return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, false, true>, p)
-                        : cudaLaunchKernelEx(&cfg, combine_kernel<false, false, true>, p);
-    }
-    if (fp8_cache)
-        return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, true, false>, p)
-                        : cudaLaunchKernelEx(&cfg, combine_kernel<false, true, false>, p);
-    return out_bf16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, false, false>, p)
-                    : cudaLaunchKernelEx(&cfg, combine_kernel<false, false, false>, p);
+    // slots per round trip: 8 in the cascade variant (which also folds prefix
+    // partials) and where units average under 8 segments, else 10 (at most 112
+    // registers either way)
+    const bool wide = !p.cascade && static_cast<long long>(p.num_workers) > 8 * units;
+    auto kernel = [&](auto ob, auto f8) -> const void* {
+        constexpr bool O = decltype(ob)::value, F = decltype(f8)::value;
+        if (p.cascade) return reinterpret_cast<const void*>(&combine_kernel<O, F, true, 8>);
+        return wide ? reinterpret_cast<const void*>(&combine_kernel<O, F, false, 10>)
+                    : reinterpret_cast<const void*>(&combine_kernel<O, F, false, 8>);
+    };
+    using T = std::true_type;
+    using Fa = std::false_type;
+    const void* fn = out_bf16 ? (fp8_cache ? kernel(T{}, T{}) : kernel(T{}, Fa{}))
+                              : (fp8_cache ? kernel(Fa{}, T{}) : kernel(Fa{}, Fa{}));
+    void* args[] = {const_cast<DecodeParams*>(&p)};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace pa
