@@ -212,6 +212,11 @@ def build_step(w: W.Workload, pa, ws, outs, layers_caches, decode_only_kernels=F
         kc, vc = layers_caches[layer]
         ks = w.k_scale[layer:layer + 1] if w.k_scale is not None else None
         vs = w.v_scale[layer:layer + 1] if w.v_scale is not None else None
+        if w.is_decode_only and w.num_new_tokens and not cascade:
+            # a decode step: the new tokens' slot write fused into the decode (both graphs)
+            pa.pa_decode_append(outs[layer], w.q[layer], w.k_new[layer], w.v_new[layer], w.slot_mapping, kc, vc,
+                                w.block_tables, w.seq_lens, w.scale, ws, ks, vs)
+            continue
         if w.num_new_tokens and not decode_only_kernels:
             pa.pa_reshape_and_cache(w.k_new[layer], w.v_new[layer], kc, vc, w.slot_mapping, ks, vs)
         if w.is_decode_only and cascade:
@@ -255,8 +260,10 @@ def run_ours(args, rank, world, local):
     step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, cascade=cascade))
     decode_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, decode_only_kernels=True,
                                               cascade=cascade))
-    # per layer: the slot write, the attention kernel and its combine, the chunk kernel of a mixed batch
-    launches_per_step = w.num_layers * ((1 if w.num_new_tokens else 0) + 2 +
+    # per layer: the slot write (fused into the decode kernel in a decode step), the
+    # attention kernel and its combine, the chunk kernel of a mixed batch or cascade
+    fused = w.is_decode_only and w.num_new_tokens and not cascade
+    launches_per_step = w.num_layers * ((1 if w.num_new_tokens and not fused else 0) + 2 +
                                         (0 if w.is_decode_only and not cascade else 1))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     unique_bytes = sum(c.numel() * c.element_size() * 2 for c in w.k_cache)
@@ -362,9 +369,10 @@ def run_ours(args, rank, world, local):
             "last_block_waste": last_block_waste(w),
             "kv_bytes_per_step": kv_bytes,
             "launch": f"one CUDA graph per step: {w.num_layers} x ("
-                      + ("pa_reshape_and_cache + " if w.num_new_tokens else "")
-                      + (("pa_decode_shared_prefix" if cascade else "pa_decode") if w.is_decode_only
-                         else "pa_mixed") + ")",
+                      + ("pa_decode_append (slot write fused into the decode)" if fused else
+                         ("pa_reshape_and_cache + " if w.num_new_tokens else "")
+                         + (("pa_decode_shared_prefix" if cascade else "pa_decode") if w.is_decode_only
+                            else "pa_mixed")) + ")",
             "l2": ("L2 flushed between steps" if flush else
                    f"inputs larger than L2 ({unique_bytes / 1e9:.2f} GB of cache vs {l2 / 1e6:.0f} MB L2)"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -373,7 +381,8 @@ def run_ours(args, rank, world, local):
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / hbm_peak, 2),
         "roofline": {
-            "kernel": "pa_decode_shared_prefix (unique bytes: prefix once + suffixes)" if cascade else "pa_decode",
+            "kernel": "pa_decode_shared_prefix (unique bytes: prefix once + suffixes)" if cascade else
+                      ("pa_decode_append" if fused else "pa_decode"),
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": hbm_peak,

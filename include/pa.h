@@ -178,6 +178,33 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                     const float* k_scale, const float* v_scale, void* workspace,
                     size_t workspace_bytes, pa_stream_t stream);
 
+/*
+ * One decode step in one pass: pa_reshape_and_cache of each sequence's new token
+ * followed by pa_decode, with the same results (the cache bytes bit for bit, the
+ * outputs exactly) [P1 s.3: each step appends one token per running request and
+ * attends over all of them; s.4 slot mapping].  The warps that read a sequence's
+ * last 16 keys store its new token into the cache slot first, so the slot write
+ * costs no separate launch.
+ *
+ *   k_new, v_new   device, [num_seqs][num_kv_heads][128] of q_dtype, 16-byte aligned
+ *   slot_mapping   device, int64 [num_seqs]: slot_mapping[s] must be the slot of
+ *                  position seq_lens[s] - 1 of sequence s (block
+ *                  block_tables[s][(seq_lens[s] - 1) / block_size], offset
+ *                  (seq_lens[s] - 1) % block_size), or negative (padding: nothing is
+ *                  written).  Another slot, or a non-negative slot for an empty
+ *                  sequence, is recorded as PA_ERR_OUT_OF_RANGE and not written.
+ *   k_cache, v_cache written at those slots (FP8 with the pa_reshape_and_cache rule)
+ * The block holding a new token must belong to its sequence alone (copy it first
+ * when it is shared, see pa_pool_copy_on_write).  Other arguments as pa_decode.
+ */
+PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int num_blocks, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                                  const float* k_scale, const float* v_scale, void* workspace,
+                                  size_t workspace_bytes, pa_stream_t stream);
+
 /* pa_decode with an explicit worker count (1 .. pa_default_workers(); 0 = the
  * default).  Fewer workers means longer ranges per worker and fewer split
  * points; results agree with pa_decode to rounding. */

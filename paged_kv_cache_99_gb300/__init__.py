@@ -66,6 +66,8 @@ def _lib():
     lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
     lib.pa_decode.restype = I
     lib.pa_decode_ex.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, I, P]
+    lib.pa_decode_append.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
+    lib.pa_decode_append.restype = I
     lib.pa_decode_ex.restype = I
     lib.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
     lib.pa_decode_shared_prefix.restype = I
@@ -202,6 +204,33 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, workspace
                              _DTYPE[q.dtype], _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale), _ptr(v_scale),
                              _ptr(workspace), workspace.numel(), int(num_workers), _stream(stream))
     _check(st, "pa_decode")
+
+
+def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, seq_lens, scale, workspace,
+                     k_scale=None, v_scale=None, stream=None):
+    """pa_reshape_and_cache of one new token per sequence (k_new, v_new [B, H_kv, 128] at
+    slot_mapping[B], int64, the slot of position seq_lens[s] - 1) fused with pa_decode."""
+    _need(q, "q", (torch.bfloat16, torch.float16))
+    _need(out, "out", (q.dtype,))
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, (q.dtype,))
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, tuple(_DTYPE))
+    _need(slot_mapping, "slot_mapping", (torch.int64,))
+    _need(block_tables, "block_tables", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(workspace, "workspace", (torch.uint8,))
+    B, Hq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    if (out.shape != q.shape or block_tables.shape[0] != B or seq_lens.shape != (B,) or
+            k_new.shape != (B, Hkv, d) or v_new.shape != k_new.shape or slot_mapping.shape != (B,)):
+        raise ValueError("shape mismatch")
+    st = _lib().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+                                 _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv,
+                                 d, bs, nb, float(scale), _DTYPE[q.dtype],
+                                 _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale), _ptr(v_scale),
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "pa_decode_append")
 
 
 def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, prefix_blocks, scale, workspace,

@@ -101,7 +101,7 @@ __device__ __forceinline__ T shfl(T v, int src) {
 
 }  // namespace
 
-template <int Kind, bool QBf16>
+template <int Kind, bool QBf16, bool Append>
 __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p) {
     using Cfg = DecodeCfg<Kind>;
     constexpr bool kFp8 = Cfg::kFp8;
@@ -185,6 +185,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         if (!eligible(s)) continue;
         const int n = p.seq_lens[s];
         if (threadIdx.x == 0 && n > p.max_blocks * p.block_size) atomicOr(p.status, kDevErrRange);
+        // a fused slot write needs a token to write: an empty sequence takes padding
+        if (threadIdx.x == 0 && p.append && n <= 0 && p.slots[s] >= 0) atomicOr(p.status, kDevErrRange);
         if (n > 0) continue;
         const int row = mixed ? p.query_start_loc[s] : s;
         uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
@@ -235,7 +237,19 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
 
     // ---- producer: block-table window + TMA issue ----
     int tbl_s = -1, tbl_j0 = -1, tbl = 0;
-    int pn_s = -1, pn_ent = 0;                  // producer: sequence whose table entries are counted
+    int pn_s = -1, pn_ent = 0, pn_n = 0;        // producer: sequence whose table entries are counted
+    // fused slot write: the lane's 16 bytes of the next new-token row (k_new / v_new
+    // row s H_kv + h), fetched when the unit holding it is issued and stored when it
+    // is consumed, so that neither waits for the load
+    const int part = lane & 15;
+    const bool part_v = lane >= 16;
+    const uint16_t* new_rows = part_v ? p.v_new : p.k_new;
+    auto load_new = [&](int row) -> uint4 {
+        return __ldg(reinterpret_cast<const uint4*>(new_rows + static_cast<size_t>(row) * kHeadDim) + part);
+    };
+    int pf_row = -1, pf_want = 0, pf_dst = 0;       // row fetched ahead (-1: none pending)
+    long long pf_slot = -1;
+    uint4 pf_x = make_uint4(0, 0, 0, 0);
     auto issue = [&](const Cursor& c, int k) {
         // unit ja (16 keys) of the sequence: with blocks of 16 or 32 tokens it lies in
         // table entry 16 ja / bs at row offset 16 ja mod bs; with 8-token blocks it
@@ -244,7 +258,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         const int bs = p.block_size, bsh = p.block_shift;
         if (c.s != pn_s) {
             pn_s = c.s;
-            pn_ent = (max(p.seq_lens[c.s], 0) + bs - 1) >> bsh;
+            pn_n = max(p.seq_lens[c.s], 0);
+            pn_ent = (pn_n + bs - 1) >> bsh;
         }
         const int ti = (ja * kBlockSize) >> bsh;
         if (c.s != tbl_s || (ti & ~31) != tbl_j0) {
@@ -264,6 +279,18 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         const int h = c.uh / p.head_groups;
         const int y0 = ((phys0 * p.num_kv_heads + h) << bsh) + ((ja * kBlockSize) & (bs - 1));
         const int y1 = (phys1 * p.num_kv_heads + h) << bsh;
+        if (Append && ja == ((pn_n - 1) >> 4) && pf_row < 0) {
+            // the sequence's last 16 keys hold its new token (position n - 1): fetch the
+            // lane's part of its row, its slot and where it belongs now, for the
+            // consumer to store when this unit is consumed
+            const int e = (pn_n - 1) >> bsh;                          // its table entry
+            const int ph = e == ti ? phys0 : phys1;
+            pf_row = c.s * p.num_kv_heads + h;
+            pf_x = load_new(pf_row);
+            pf_slot = __ldg(p.slots + c.s);
+            pf_want = ph * bs + ((pn_n - 1) & (bs - 1));
+            pf_dst = ((ph * p.num_kv_heads + h) << bsh) + ((pn_n - 1) & (bs - 1));
+        }
         if (lane == 0) {
             const int st = k % NS;
             const uint32_t bar = my_bars + 8 * st;
@@ -375,6 +402,60 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         const uint32_t kt = my_tiles + st * STAGE;
         const uint32_t vt = kt + TILE;
         const int valid = min(kBlockSize, n_cur - (C.j + p.first_block) * kBlockSize);
+        if constexpr (Append) {
+            if (C.j + p.first_block == ((n_cur - 1) >> 4)) {
+                // this unit holds the sequence's new token: store it into its slot and
+                // over its row of the tile just copied (the copy may predate the store)
+                const int h = C.uh / p.head_groups;
+                const int nrow = C.s * p.num_kv_heads + h;
+                uint4 x;
+                long long slot;
+                int want, dst;
+                bool ok_row = true;
+                if (nrow == pf_row) {
+                    x = pf_x;
+                    slot = pf_slot;
+                    want = pf_want;
+                    dst = pf_dst;
+                    pf_row = -1;
+                } else {   // a second new token inside the ring: fetched now
+                    const int e = (n_cur - 1) >> p.block_shift;
+                    const int ph = __ldg(p.block_tables + static_cast<size_t>(C.s) * p.max_blocks + e);
+                    ok_row = static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks);
+                    x = load_new(nrow);
+                    slot = __ldg(p.slots + C.s);
+                    want = ph * p.block_size + ((n_cur - 1) & (p.block_size - 1));
+                    dst = ((ph * p.num_kv_heads + h) << p.block_shift) + ((n_cur - 1) & (p.block_size - 1));
+                }
+                if (slot >= 0) {
+                    if (!ok_row || slot != want) {
+                        if (lane == 0) atomicOr(p.status, kDevErrRange);
+                    } else {
+                        const uint32_t r = static_cast<uint32_t>((n_cur - 1) & 15);    // row in the tile
+                        const uint32_t tile = part_v ? vt : kt;
+                        if constexpr (!kFp8) {
+                            uint16_t* gdst = static_cast<uint16_t*>(part_v ? p.v_cache_w : p.k_cache_w) +
+                                             static_cast<size_t>(dst) * kHeadDim;
+                            reinterpret_cast<uint4*>(gdst)[part] = x;
+                            const uint32_t a = tile + ((part >> 3) << 11) + (r << 7) + (((part & 7) ^ (r & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x.x), "r"(x.y),
+                                         "r"(x.z), "r"(x.w) : "memory");
+                        } else {
+                            const float sc = __ldg((part_v ? p.v_scale : p.k_scale) + h * p.scale_stride);
+                            const uint32_t lo = e4m3_pair<QBf16>(x.x, sc) | (e4m3_pair<QBf16>(x.y, sc) << 16);
+                            const uint32_t hi = e4m3_pair<QBf16>(x.z, sc) | (e4m3_pair<QBf16>(x.w, sc) << 16);
+                            uint8_t* gdst = static_cast<uint8_t*>(part_v ? p.v_cache_w : p.k_cache_w) +
+                                            static_cast<size_t>(dst) * kHeadDim;
+                            reinterpret_cast<uint2*>(gdst)[part] = make_uint2(lo, hi);
+                            const uint32_t a = tile + (r << 7) + ((((part >> 1) ^ (r & 7))) << 4) + ((part & 1) << 3);
+                            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(lo), "r"(hi) : "memory");
+                        }
+                        fence_proxy_async_smem();     // before a later copy into this stage
+                    }
+                }
+                __syncwarp();
+            }
+        }
 
         // ---- S^T = K . Q^T : rows = 16 keys, cols = 8 heads ----
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -544,12 +625,21 @@ template <int Kind, bool QBf16>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
-    decode_body<Kind, QBf16>(kmap, vmap, p);
+    decode_body<Kind, QBf16, false>(kmap, vmap, p);
     // Overlapping a chunk launch of the same call (which neither reads what this grid
     // writes nor writes what it reads): the last CTA alone waits for it before exiting,
     // so that this grid, and the combine chained behind it, completes after it while
     // every other CTA frees its SM as soon as its range is done.
     if (p.overlap_prior && blockIdx.x == gridDim.x - 1) grid_dependency_wait();
+}
+
+// The same with the new tokens' slot write fused in (pa_decode_append), held to the
+// plain kernel's 136 registers so that two CTAs and a combine CTA still share an SM.
+template <int Kind, bool QBf16>
+__global__ void __maxnreg__(136)
+    decode_append_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                         const DecodeParams p) {
+    decode_body<Kind, QBf16, true>(kmap, vmap, p);
 }
 
 
@@ -748,15 +838,16 @@ __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
 
 namespace {
 template <int Kind, bool QBf16>
-void* kernel_ptr() {
-    return reinterpret_cast<void*>(&decode_kernel<Kind, QBf16>);
+void* kernel_ptr(bool append) {
+    return append ? reinterpret_cast<void*>(&decode_append_kernel<Kind, QBf16>)
+                  : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16>);
 }
 
-void* decode_fn(CacheKind kind, bool q_bf16) {
+void* decode_fn(CacheKind kind, bool q_bf16, bool append) {
     switch (kind) {
-        case kKindBf16: return kernel_ptr<kKindBf16, true>();
-        case kKindFp16: return kernel_ptr<kKindFp16, false>();
-        case kKindFp8: return q_bf16 ? kernel_ptr<kKindFp8, true>() : kernel_ptr<kKindFp8, false>();
+        case kKindBf16: return kernel_ptr<kKindBf16, true>(append);
+        case kKindFp16: return kernel_ptr<kKindFp16, false>(append);
+        case kKindFp8: return q_bf16 ? kernel_ptr<kKindFp8, true>(append) : kernel_ptr<kKindFp8, false>(append);
     }
     return nullptr;
 }
@@ -776,21 +867,21 @@ size_t decode_smem_bytes(CacheKind kind, int num_seqs) {
     return 1024 + static_cast<size_t>(tile_area_bytes(kind)) + static_cast<size_t>(num_seqs + 1) * 4;
 }
 
-cudaError_t decode_prepare(CacheKind kind, bool q_bf16, size_t max_smem) {
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, size_t max_smem) {
     // the largest request a call can make (kMaxSeqs sequences), within what the
     // device allows next to the kernel's static shared memory
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, decode_fn(kind, q_bf16));
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_fn(kind, q_bf16, append));
     if (e != cudaSuccess) return e;
     size_t want = decode_smem_bytes(kind, kMaxSeqs);
     const size_t cap = max_smem > fa.sharedSizeBytes ? max_smem - fa.sharedSizeBytes : 0;
     if (want > cap) want = cap;
-    return cudaFuncSetAttribute(decode_fn(kind, q_bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(decode_fn(kind, q_bf16, append), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(want));
 }
 
-cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_fn(kind, q_bf16),
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, size_t smem, int* ctas_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_fn(kind, q_bf16, append),
                                                          kDecodeWarps * 32, smem);
 }
 
@@ -806,14 +897,10 @@ cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    switch (kind) {
-        case kKindBf16: return cudaLaunchKernelEx(&cfg, decode_kernel<kKindBf16, true>, kmap, vmap, p);
-        case kKindFp16: return cudaLaunchKernelEx(&cfg, decode_kernel<kKindFp16, false>, kmap, vmap, p);
-        case kKindFp8:
-            return q_bf16 ? cudaLaunchKernelEx(&cfg, decode_kernel<kKindFp8, true>, kmap, vmap, p)
-                          : cudaLaunchKernelEx(&cfg, decode_kernel<kKindFp8, false>, kmap, vmap, p);
-    }
-    return cudaErrorInvalidValue;
+    void* args[] = {const_cast<CUtensorMap*>(&kmap), const_cast<CUtensorMap*>(&vmap), const_cast<DecodeParams*>(&p)};
+    const void* fn = decode_fn(kind, q_bf16, p.append != 0);
+    if (!fn) return cudaErrorInvalidValue;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p, int max_ctas,

@@ -23,13 +23,13 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     size_t max_smem_optin = 0;
-    bool decode_prepared[3][2] = {};
+    bool decode_prepared[3][2][2] = {};
     bool chunk_prepared[3][2] = {};
 };
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
-std::map<std::tuple<int, int, int, size_t>, int> g_occupancy;
+std::map<std::tuple<int, int, int, int, size_t>, int> g_occupancy;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 thread_local char g_last_error[256] = "";
@@ -167,26 +167,28 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
                       void* workspace, size_t workspace_bytes, int num_workers, int num_blocks, int block_size,
                       int total_rows, cudaStream_t stream, bool overlap_prior = false, bool cascade = false,
                       int first_block = 0, int prefix_splits = 1, const float* prefix_o_extra = nullptr,
-                      const float* prefix_ml_extra = nullptr) {
+                      const float* prefix_ml_extra = nullptr, const void* k_new = nullptr,
+                      const void* v_new = nullptr, const int64_t* slots = nullptr) {
     int dev = 0;
     DeviceState* st = device_state(&dev);
     if (!st) return PA_ERR_CUDA;
     const CacheKind kind = kind_of(cache_dtype);
     const bool q_bf16 = q_dtype == PA_BF16;
+    const bool append = slots != nullptr;
     const size_t smem = decode_smem_bytes(kind, num_seqs);
     if (smem + 1024 > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
     int ctas = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!st->decode_prepared[kind][q_bf16]) {
-            cudaError_t e = decode_prepare(kind, q_bf16, st->max_smem_optin);
+        if (!st->decode_prepared[kind][q_bf16][append]) {
+            cudaError_t e = decode_prepare(kind, q_bf16, append, st->max_smem_optin);
             if (e != cudaSuccess) return fail("cudaFuncSetAttribute(decode)", e);
-            st->decode_prepared[kind][q_bf16] = true;
+            st->decode_prepared[kind][q_bf16][append] = true;
         }
-        auto key = std::make_tuple(dev, static_cast<int>(kind), static_cast<int>(q_bf16), smem);
+        auto key = std::make_tuple(dev, static_cast<int>(kind), static_cast<int>(q_bf16), static_cast<int>(append), smem);
         auto it = g_occupancy.find(key);
         if (it == g_occupancy.end()) {
-            cudaError_t e = decode_occupancy(kind, q_bf16, smem, &ctas);
+            cudaError_t e = decode_occupancy(kind, q_bf16, append, smem, &ctas);
             if (e != cudaSuccess) return fail("cudaOccupancyMaxActiveBlocksPerMultiprocessor(decode)", e);
             if (ctas <= 0) return fail_msg("decode kernel does not fit on an SM");
             g_occupancy[key] = ctas;
@@ -241,6 +243,12 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.prefix_splits = prefix_splits;
     p.prefix_o_extra = prefix_o_extra;
     p.prefix_ml_extra = prefix_ml_extra;
+    p.append = slots != nullptr ? 1 : 0;
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
+    p.slots = slots;
+    p.k_cache_w = const_cast<void*>(k_cache);
+    p.v_cache_w = const_cast<void*>(v_cache);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
@@ -543,6 +551,25 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
                        workspace_bytes, workers, num_blocks, block_size, num_seqs, cs, prefix_units > 0, true,
                        prefix_units, splits, o_extra, ml_extra);
+}
+
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, void* k_cache, void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                           pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                           void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+    pa_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                       scale, q_dtype, cache_dtype, k_scale, v_scale, workspace);
+    if (s != PA_OK) return s;
+    if (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                       num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
+                       workspace_bytes, 0, num_blocks, block_size, num_seqs, reinterpret_cast<cudaStream_t>(stream),
+                       false, false, 0, 1, nullptr, nullptr, k_new, v_new, slot_mapping);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -72,6 +72,16 @@ struct DecodeParams {
     int prefix_splits;                // prefix partials per row (key segments of the prefix)
     const float* prefix_o_extra;      // [prefix_splits - 1][num_seqs][num_q_heads][128]
     const float* prefix_ml_extra;     // [prefix_splits - 1][num_seqs][num_q_heads][2]
+    // Slot write fused into the decode: the new token of sequence s (row s of k_new /
+    // v_new, [num_seqs][num_kv_heads][128] in the query's 16-bit type) goes to slot
+    // slots[s], which must be the slot of position seq_lens[s] - 1 (a negative slot
+    // is padding); the warps that read the sequence's last 16 keys write it first.
+    int append;
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    const int64_t* slots;
+    void* k_cache_w;
+    void* v_cache_w;
     float scale_log2;                 // softmax scale * log2(e)
     unsigned long long timeout_ns;    // bound of every barrier wait
 };
@@ -133,8 +143,8 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 
 // Decode kernels: dynamic shared memory for num_seqs sequences.
 size_t decode_smem_bytes(CacheKind kind, int num_seqs);
-cudaError_t decode_prepare(CacheKind kind, bool q_bf16, size_t max_smem);
-cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, size_t smem, int* ctas_per_sm);
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, size_t max_smem);
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, size_t smem, int* ctas_per_sm);
 cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, const DecodeParams& p, int grid, size_t smem,
                           cudaStream_t stream);

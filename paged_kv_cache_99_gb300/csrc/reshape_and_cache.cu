@@ -21,24 +21,6 @@ namespace pa {
 
 namespace {
 
-// Codes of the two 16-bit source elements packed in `word` (low half first):
-// e4m3(fl32(x) / scale) with satfinite rounding; a NaN quotient takes the sign
-// bit of its source element (read from the raw bits: the fp16 -> fp32
-// conversion does not keep NaN signs), a zero code the sign of the quotient.
-template <bool SrcBf16>
-__device__ __forceinline__ uint32_t e4m3_pair(uint32_t word, float scale) {
-    const float lo = __fdiv_rn(to_float<SrcBf16>(word & 0xffffu), scale);
-    const float hi = __fdiv_rn(to_float<SrcBf16>(word >> 16), scale);
-    uint16_t y;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(y) : "f"(hi), "f"(lo));
-    uint32_t c_lo = y & 0xffu, c_hi = y >> 8;
-    if (isnan(lo)) c_lo = ((word >> 8) & 0x80u) | 0x7fu;
-    else if ((c_lo & 0x7fu) == 0) c_lo = signbit(lo) ? 0x80u : 0u;
-    if (isnan(hi)) c_hi = ((word >> 24) & 0x80u) | 0x7fu;
-    else if ((c_hi & 0x7fu) == 0) c_hi = signbit(hi) ? 0x80u : 0u;
-    return c_lo | (c_hi << 8);
-}
-
 template <bool SrcBf16, bool Fp8>
 __global__ void __launch_bounds__(256)
     reshape_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, void* k_cache,
