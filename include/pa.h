@@ -123,11 +123,13 @@ PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cach
 /*
  * Bytes of workspace pa_decode / pa_mixed need on the CURRENT device for
  * num_seqs sequences (the default worker count depends on the device's SM
- * count).  The workspace is caller-owned device memory, 256-byte aligned; its
- * contents need no initialisation (the first word is the device status word,
- * see pa_read_device_status; the rest is scratch each call overwrites before
- * reading).  One workspace must not be used by two calls that may overlap on
- * the GPU.  Returns 0 for invalid arguments.
+ * count).  The workspace is caller-owned device memory, 256-byte aligned.  Its
+ * first 256 bytes must be zero before the first call: they hold the device
+ * status word (the first word, see pa_read_device_status) and the counter from
+ * which decode warps claim the last pieces of work, which every call leaves
+ * ready for the next.  The rest is scratch each call overwrites before reading
+ * and needs no initialisation.  One workspace must not be used by two calls
+ * that may overlap on the GPU.  Returns 0 for invalid arguments.
  */
 PA_API size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
 

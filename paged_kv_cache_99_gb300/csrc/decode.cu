@@ -75,6 +75,56 @@ __device__ __forceinline__ int worker_of(long long f, long long T, int W) {
     return static_cast<int>(((f + 1) * W - 1) / T);
 }
 
+// How the flattened order [0, T) is cut.  Ranges 0 .. W-1 are static, one per
+// worker, over [0, Ts); ranges W .. W+P-1 are pieces of S blocks over [Ts, T) that
+// workers claim from a counter once their own range is done (SMs do not all stream
+// at one rate, and the slow ones would otherwise set the end of the launch).  Range
+// indices grow along the flattened order, so the ranges covering a unit are
+// consecutive and a partial's slot is range + unit.
+struct Split {
+    int T, Ts, W, P, S;        // flattened indices fit in 32 bits (checked on the host)
+    __device__ int range_of(int f) const { return f < Ts ? worker_of(f, Ts, W) : W + (f - Ts) / S; }
+};
+
+// dyn256 / 256 of the blocks go to pieces of an eighth of a static range (at least
+// kMinPiece blocks), at most one piece per worker, when ranges are long enough to
+// cut (kMinPieceRange blocks: a piece of a short range takes a warp as long as a
+// range); every worker gets a non-empty static range or none.
+__device__ __forceinline__ Split make_split(int T, int workers, int dyn256) {
+    Split sp;
+    sp.T = T;
+    const int per = T / max(workers, 1);
+    const int dyn = per < kMinPieceRange ? 0 : static_cast<int>(static_cast<long long>(T) * dyn256 / 256);
+    const int P = min(workers, dyn / max(kMinPiece, per / 8));
+    if (P <= 0) {
+        sp.Ts = T;
+        sp.P = 0;
+        sp.S = 1;
+    } else {
+        sp.S = (dyn + P - 1) / P;
+        sp.P = (dyn + sp.S - 1) / sp.S;
+        sp.Ts = T - dyn;
+    }
+    sp.W = min(workers, sp.Ts);
+    return sp;
+}
+
+// Cursor at flattened index f: the sequence s with cum[s] <= f < cum[s + 1].
+__device__ __forceinline__ Cursor locate(int f, const int* cum, int B, int UH) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid] <= f) lo = mid; else hi = mid;
+    }
+    Cursor c;
+    c.s = lo;
+    c.nb = (cum[lo + 1] - cum[lo]) / UH;
+    const int rem = f - cum[lo];
+    c.uh = rem / c.nb;
+    c.j = rem % c.nb;
+    return c;
+}
+
 // Decode rows of a mixed batch are the sequences with q_len == 1 (whose row lies
 // inside q: a malformed query_start_loc is recorded by the prologue and its rows skipped).
 __device__ __forceinline__ bool decode_row(const DecodeParams& p, int s) {
@@ -101,7 +151,7 @@ __device__ __forceinline__ T shfl(T v, int src) {
 
 }  // namespace
 
-template <int Kind, bool QBf16, bool Append>
+template <int Kind, bool QBf16, bool Append, bool Dyn>
 __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p) {
     using Cfg = DecodeCfg<Kind>;
     constexpr bool kFp8 = Cfg::kFp8;
@@ -201,31 +251,43 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         for (int i = threadIdx.x; i <= B; i += blockDim.x) p.plan[i] = cum[i];
     }
 
-    const long long T = cum[B];
-    // never more workers than blocks, so that every worker's range is non-empty and
-    // the workers covering a unit are exactly worker_of(first) .. worker_of(last)
-    const int W = static_cast<int>(min(static_cast<long long>(p.num_workers), T));
+    const int T = cum[B];
+    if (T == 0) return;
+    const Split sp = make_split(T, p.num_workers, p.dyn256);
     const int wid = blockIdx.x * kDecodeWarps + warp;
-    if (wid >= W || T == 0) return;
-    const long long f0 = T * wid / W;
-    const long long f1 = T * (wid + 1) / W;
-    if (f0 == f1) return;
-    const int nblk = static_cast<int>(f1 - f0);
-
-    // locate f0: sequence with cum[s] <= f0 < cum[s+1]
-    Cursor start;
-    {
-        int lo = 0, hi = B;
-        while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (cum[mid] <= f0) lo = mid; else hi = mid;
-        }
-        start.s = lo;
-        start.nb = (cum[lo + 1] - cum[lo]) / UH;
-        const int rem = static_cast<int>(f0 - cum[lo]);
-        start.uh = rem / start.nb;
-        start.j = rem % start.nb;
+    if (wid >= p.num_workers) return;
+    // pieces are numbered from the counter's value when this call began (the
+    // previous call's combine set claim[1] to the counter's final value)
+    const unsigned claim_base = __ldcg(p.claim + 1);
+    // a claim is sent kClaimAhead blocks before the producer needs it, so that the
+    // atomic (all warps reach the end of their static ranges at about the same time)
+    // returns while the ring still streams
+    unsigned claim_got = 0;
+    bool claim_sent = false;
+    auto send_claim = [&]() {
+        if (lane == 0) claim_got = atomicAdd(p.claim, 1u);
+        claim_sent = true;
+    };
+    auto claim = [&](int& lo, int& hi, int& ri) -> bool {
+        if (!claim_sent) send_claim();
+        claim_sent = false;
+        const unsigned k = shfl(claim_got, 0) - claim_base;     // modulo 2^32
+        if (k >= static_cast<unsigned>(sp.P)) return false;
+        lo = sp.Ts + static_cast<int>(k) * sp.S;
+        hi = min(sp.T, lo + sp.S);
+        ri = sp.W + static_cast<int>(k);
+        return true;
+    };
+    // the consumer's range [c_lo, c_hi), index c_ri: first the worker's static range
+    int c_lo = 0, c_hi = 0, c_ri = 0;
+    if (wid < sp.W) {
+        c_ri = wid;
+        c_lo = static_cast<int>(static_cast<long long>(sp.Ts) * wid / sp.W);
+        c_hi = static_cast<int>(static_cast<long long>(sp.Ts) * (wid + 1) / sp.W);
+    } else if (!Dyn || !claim(c_lo, c_hi, c_ri)) {
+        return;
     }
+    const Cursor start = locate(c_lo, cum, B, UH);
 
     // per-lane fragment geometry
     const int g = lane >> 2;           // MMA group row
@@ -329,12 +391,40 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         }
     };
 
+    // producer: next flattened index p_f of its range [.., p_hi); a range it claims is
+    // handed to the consumer (at most one waits: a piece is longer than the ring)
     Cursor P = start;
     int kp = 0;
-    for (; kp < NS && kp < nblk; ++kp) {
+    int p_f = c_lo, p_hi = c_hi;
+    bool p_done = sp.P == 0, nx_valid = false;      // nothing to claim: no atomics at all
+    int nx_lo = 0, nx_hi = 0, nx_ri = 0;
+    auto produce = [&]() {
+        if constexpr (!Dyn) {
+            if (p_f == p_hi) return;
+        } else if (!p_done && !claim_sent && p_hi - p_f <= kClaimAhead) {
+            send_claim();
+        }
+        if (p_f == p_hi) {
+            if (p_done || nx_valid) return;
+            int lo, hi, ri;
+            if (!claim(lo, hi, ri)) {
+                p_done = true;
+                return;
+            }
+            nx_lo = lo;
+            nx_hi = hi;
+            nx_ri = ri;
+            nx_valid = true;
+            p_f = lo;
+            p_hi = hi;
+            P = locate(lo, cum, B, UH);
+        }
         issue(P, kp);
         cursor_advance(P, cum, B, UH);
-    }
+        ++kp;
+        ++p_f;
+    };
+    for (int i = 0; i < NS; ++i) produce();
 
     // FP8 scales of the current unit's KV head (set at each segment start)
     float s_log2 = p.scale_log2, vscale = 1.0f;
@@ -346,7 +436,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     int n_cur = 0, row_cur = 0;
     bool open = false;
 
-    for (int kc = 0; kc < nblk; ++kc) {
+    int c_f = c_lo;
+    for (int kc = 0; kc < kp; ++kc) {
         if (!open) {
             // ---- segment start: query fragments of this unit ----
             open = true;
@@ -558,14 +649,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         __syncwarp();
 
         // refill the stage just consumed
-        if (kp < nblk) {
-            issue(P, kp);
-            cursor_advance(P, cum, B, UH);
-            ++kp;
-        }
+        produce();
 
         // ---- segment end: unit finished or range finished ----
-        if (C.j == C.nb - 1 || kc == nblk - 1) {
+        if (C.j == C.nb - 1 || c_f == c_hi - 1) {
             open = false;
 #pragma unroll
             for (int o2 = 4; o2 < 32; o2 <<= 1) {
@@ -573,12 +660,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
                 l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
             }
             const int u = C.s * UH + C.uh;
-            const long long fu = cum[C.s] + static_cast<long long>(C.uh) * C.nb;
-            // a unit one worker covers is written directly, unless a prefix partial waits for it
-            const bool write = !p.cascade && worker_of(fu, T, W) == worker_of(fu + C.nb - 1, T, W);
+            const int fu = cum[C.s] + C.uh * C.nb;
+            // a unit one range covers is written directly, unless a prefix partial waits for it
+            const bool write = !p.cascade && sp.range_of(fu) == sp.range_of(fu + C.nb - 1);
             if (!write) {
-                // unit shared with other workers: plain partial store, merged by combine_kernel
-                const int slot = wid + u;
+                // unit shared with other ranges: plain partial store, merged by combine_kernel
+                const int slot = c_ri + u;
                 float4* part = p.partial + static_cast<size_t>(slot) * 8 * 32;
 #pragma unroll
                 for (int dt = 0; dt < 8; ++dt) part[dt * 32 + lane] = make_float4(o[dt][0], o[dt][1], o[dt][2], o[dt][3]);
@@ -617,15 +704,29 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
                 }
             }
         }
-        cursor_advance(C, cum, B, UH);
+        if (++c_f == c_hi && Dyn) {
+            if (!nx_valid) continue;          // the loop ends once every issued block is consumed
+            c_lo = nx_lo;
+            c_hi = nx_hi;
+            c_ri = nx_ri;
+            nx_valid = false;
+            c_f = c_lo;
+            C = locate(c_lo, cum, B, UH);
+            open = false;
+        } else {
+            cursor_advance(C, cum, B, UH);
+        }
     }
 }
 
-template <int Kind, bool QBf16>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
+// At most 136 registers per thread: two CTAs (128 threads each) and a combine CTA
+// (256 threads, at most 112) share an SM, so the combine is resident, past its
+// prologue, while the decode grid drains.
+template <int Kind, bool QBf16, bool Dyn>
+__global__ void __maxnreg__(136)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
-    decode_body<Kind, QBf16, false>(kmap, vmap, p);
+    decode_body<Kind, QBf16, false, Dyn>(kmap, vmap, p);
     // Overlapping a chunk launch of the same call (which neither reads what this grid
     // writes nor writes what it reads): the last CTA alone waits for it before exiting,
     // so that this grid, and the combine chained behind it, completes after it while
@@ -633,13 +734,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kMaxDecodeCtasPerSm)
     if (p.overlap_prior && blockIdx.x == gridDim.x - 1) grid_dependency_wait();
 }
 
-// The same with the new tokens' slot write fused in (pa_decode_append), held to the
-// plain kernel's 136 registers so that two CTAs and a combine CTA still share an SM.
-template <int Kind, bool QBf16>
+// The same with the new tokens' slot write fused in (pa_decode_append).
+template <int Kind, bool QBf16, bool Dyn>
 __global__ void __maxnreg__(136)
     decode_append_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                          const DecodeParams p) {
-    decode_body<Kind, QBf16, true>(kmap, vmap, p);
+    decode_body<Kind, QBf16, true, Dyn>(kmap, vmap, p);
 }
 
 
@@ -669,14 +769,14 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
         T = p.plan[B];
     }
     const int nb = unit_blocks_of(p, s, UH) / UH;
-    const int W = static_cast<int>(min(static_cast<long long>(p.num_workers), T));
     const bool pre = Cascade && p.first_block > 0;     // every row has a shared-prefix partial
     int wa = 0, nseg = 0;
-    if (nb > 0 && W > 0) {
-        const long long fu = lo + static_cast<long long>(uh) * nb;
-        wa = worker_of(fu, T, W);
-        const int wb = worker_of(fu + nb - 1, T, W);
-        if (wa == wb && !Cascade) return;     // its only worker wrote the output
+    if (nb > 0 && T > 0) {
+        const Split sp = make_split(static_cast<int>(T), p.num_workers, p.dyn256);
+        const int fu = static_cast<int>(lo) + uh * nb;
+        wa = sp.range_of(fu);
+        const int wb = sp.range_of(fu + nb - 1);
+        if (wa == wb && !Cascade) return;     // its only range wrote the output
         nseg = wb - wa + 1;
     } else if (!pre) {
         return;   // an empty row: the decode grid wrote its zeros
@@ -830,6 +930,11 @@ __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
     const long long units = static_cast<long long>(B) * UH;
     for (long long u = blockIdx.x; u < units; u += gridDim.x)
         combine_unit<OutBf16, Fp8Layout, Cascade, kBatch>(p, static_cast<int>(u), pre_sum);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        // every claim of this call is made: the next call numbers its pieces from here
+        grid_dependency_wait();
+        p.claim[1] = __ldcg(p.claim);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -838,16 +943,20 @@ __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
 
 namespace {
 template <int Kind, bool QBf16>
-void* kernel_ptr(bool append) {
-    return append ? reinterpret_cast<void*>(&decode_append_kernel<Kind, QBf16>)
-                  : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16>);
+void* kernel_ptr(bool append, bool dyn) {
+    if (dyn)
+        return append ? reinterpret_cast<void*>(&decode_append_kernel<Kind, QBf16, true>)
+                      : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, true>);
+    return append ? reinterpret_cast<void*>(&decode_append_kernel<Kind, QBf16, false>)
+                  : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, false>);
 }
 
-void* decode_fn(CacheKind kind, bool q_bf16, bool append) {
+void* decode_fn(CacheKind kind, bool q_bf16, bool append, bool dyn) {
     switch (kind) {
-        case kKindBf16: return kernel_ptr<kKindBf16, true>(append);
-        case kKindFp16: return kernel_ptr<kKindFp16, false>(append);
-        case kKindFp8: return q_bf16 ? kernel_ptr<kKindFp8, true>(append) : kernel_ptr<kKindFp8, false>(append);
+        case kKindBf16: return kernel_ptr<kKindBf16, true>(append, dyn);
+        case kKindFp16: return kernel_ptr<kKindFp16, false>(append, dyn);
+        case kKindFp8:
+            return q_bf16 ? kernel_ptr<kKindFp8, true>(append, dyn) : kernel_ptr<kKindFp8, false>(append, dyn);
     }
     return nullptr;
 }
@@ -867,21 +976,21 @@ size_t decode_smem_bytes(CacheKind kind, int num_seqs) {
     return 1024 + static_cast<size_t>(tile_area_bytes(kind)) + static_cast<size_t>(num_seqs + 1) * 4;
 }
 
-cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, size_t max_smem) {
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t max_smem) {
     // the largest request a call can make (kMaxSeqs sequences), within what the
     // device allows next to the kernel's static shared memory
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, decode_fn(kind, q_bf16, append));
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_fn(kind, q_bf16, append, dyn));
     if (e != cudaSuccess) return e;
     size_t want = decode_smem_bytes(kind, kMaxSeqs);
     const size_t cap = max_smem > fa.sharedSizeBytes ? max_smem - fa.sharedSizeBytes : 0;
     if (want > cap) want = cap;
-    return cudaFuncSetAttribute(decode_fn(kind, q_bf16, append), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(decode_fn(kind, q_bf16, append, dyn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(want));
 }
 
-cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, size_t smem, int* ctas_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_fn(kind, q_bf16, append),
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t smem, int* ctas_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_fn(kind, q_bf16, append, dyn),
                                                          kDecodeWarps * 32, smem);
 }
 
@@ -898,7 +1007,7 @@ cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     void* args[] = {const_cast<CUtensorMap*>(&kmap), const_cast<CUtensorMap*>(&vmap), const_cast<DecodeParams*>(&p)};
-    const void* fn = decode_fn(kind, q_bf16, p.append != 0);
+    const void* fn = decode_fn(kind, q_bf16, p.append != 0, p.dyn256 > 0);
     if (!fn) return cudaErrorInvalidValue;
     return cudaLaunchKernelExC(&cfg, fn, args);
 }

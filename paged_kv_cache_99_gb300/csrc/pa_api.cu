@@ -23,13 +23,13 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     size_t max_smem_optin = 0;
-    bool decode_prepared[3][2][2] = {};
+    bool decode_prepared[3][2][2][2] = {};
     bool chunk_prepared[3][2] = {};
 };
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
-std::map<std::tuple<int, int, int, int, size_t>, int> g_occupancy;
+std::map<std::tuple<int, int, int, int, int, size_t>, int> g_occupancy;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 thread_local char g_last_error[256] = "";
@@ -175,20 +175,33 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     const CacheKind kind = kind_of(cache_dtype);
     const bool q_bf16 = q_dtype == PA_BF16;
     const bool append = slots != nullptr;
+    // claimed pieces balance SMs that stream at different rates; they pay only where
+    // workers' ranges are long (judged from the table width: the decode grid decides
+    // from the lengths).  A mixed batch's decode grid starts beside the chunk grid,
+    // CTA by CTA, and a cascade's beside the prefix grid, whose end it rarely sets:
+    // both keep static ranges
+    const int hg0 = head_groups_of(num_q_heads, num_kv_heads);
+    const long long units_max = static_cast<long long>(num_seqs) * num_kv_heads * hg0;
+    const long long per_unit_max = (static_cast<long long>(max_blocks_per_seq) * block_size + kBlockSize - 1) / kBlockSize;
+    const long long t_max = units_max * per_unit_max;
+    const int w_default = st->sms * kMaxDecodeCtasPerSm * kDecodeWarps;
+    const int w_est = num_workers > 0 ? num_workers : w_default;
+    const bool dyn = query_start_loc == nullptr && !cascade && t_max / w_est >= kMinPieceRange;
     const size_t smem = decode_smem_bytes(kind, num_seqs);
     if (smem + 1024 > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
     int ctas = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!st->decode_prepared[kind][q_bf16][append]) {
-            cudaError_t e = decode_prepare(kind, q_bf16, append, st->max_smem_optin);
+        if (!st->decode_prepared[kind][q_bf16][append][dyn]) {
+            cudaError_t e = decode_prepare(kind, q_bf16, append, dyn, st->max_smem_optin);
             if (e != cudaSuccess) return fail("cudaFuncSetAttribute(decode)", e);
-            st->decode_prepared[kind][q_bf16][append] = true;
+            st->decode_prepared[kind][q_bf16][append][dyn] = true;
         }
-        auto key = std::make_tuple(dev, static_cast<int>(kind), static_cast<int>(q_bf16), static_cast<int>(append), smem);
+        auto key = std::make_tuple(dev, static_cast<int>(kind), static_cast<int>(q_bf16), static_cast<int>(append),
+                                   static_cast<int>(dyn), smem);
         auto it = g_occupancy.find(key);
         if (it == g_occupancy.end()) {
-            cudaError_t e = decode_occupancy(kind, q_bf16, append, smem, &ctas);
+            cudaError_t e = decode_occupancy(kind, q_bf16, append, dyn, smem, &ctas);
             if (e != cudaSuccess) return fail("cudaOccupancyMaxActiveBlocksPerMultiprocessor(decode)", e);
             if (ctas <= 0) return fail_msg("decode kernel does not fit on an SM");
             g_occupancy[key] = ctas;
@@ -235,6 +248,8 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.block_size = block_size;
     p.block_shift = block_shift_of(block_size);
     p.num_workers = W;
+    p.dyn256 = dyn ? kDynShare256 : 0;
+    p.claim = reinterpret_cast<unsigned*>(ws + lay.status_off + 8);
     p.overlap_prior = overlap_prior ? 1 : 0;
     p.cascade = cascade ? 1 : 0;
     p.first_block = cascade ? first_block : 0;
@@ -329,7 +344,8 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
                                         int workers) {
     WorkspaceLayout l;
     const size_t units = static_cast<size_t>(num_seqs) * num_kv_heads * head_groups;
-    const size_t slots = units + static_cast<size_t>(workers);
+    // ranges: one static range per worker and at most as many claimed pieces
+    const size_t slots = units + 2 * static_cast<size_t>(workers);
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
     l.status_off = 0;
     l.plan_off = 256;

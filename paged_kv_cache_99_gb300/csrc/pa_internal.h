@@ -17,6 +17,14 @@ constexpr int kBlockSize = 16;
 constexpr int kMaxSeqs = 8192;
 constexpr int kDecodeWarps = 4;        // warps per decode CTA
 constexpr int kMaxDecodeCtasPerSm = 2;
+// Decode work claimed at run time: this share (in 1/256) of the flattened blocks
+// goes to pieces of at least kMinPiece blocks (more than a ring holds) when static
+// ranges hold at least kMinPieceRange blocks; a claim is sent kClaimAhead blocks
+// before the end of the range in hand.
+constexpr int kDynShare256 = 26;
+constexpr int kMinPiece = 8;
+constexpr int kMinPieceRange = 48;
+constexpr int kClaimAhead = 4;
 constexpr int kHeadsPerGroup = 8;          // query heads handled by one decode unit (MMA N)
 // Up to this many sequences the combine kernel finds a unit's place in the flattened
 // order itself (before waiting for the decode grid); above it the decode grid
@@ -31,10 +39,11 @@ constexpr int kDevErrTimeout = 1;
 constexpr int kDevErrRange = 2;
 
 // Decode: one "unit" = (sequence, KV head, group of up to 8 query heads).  The
-// cached blocks of all units are laid end to end and cut into equal ranges, one
-// per worker (warp).  A unit covered by several workers leaves partials in the
-// slots (worker w, unit u) -> w + u, unique because both indices only grow
-// along the flattened order; the combine kernel merges them.
+// cached blocks of all units are laid end to end and cut into ranges: equal
+// static ones, one per worker (warp), then pieces the workers claim.  A unit
+// covered by several ranges leaves partials in the slots (range r, unit u) ->
+// r + u, unique because both indices only grow along the flattened order; the
+// combine kernel merges them.
 struct DecodeParams {
     void* out;
     const void* q;
@@ -59,6 +68,8 @@ struct DecodeParams {
     int block_size;                   // tokens per physical block: 8, 16 or 32
     int block_shift;                  // log2(block_size)
     int num_workers;                  // warps taking part
+    int dyn256;                       // share of the blocks in claimed pieces, in 1/256
+    unsigned* claim;                  // [0] piece counter, [1] its value when this call began
     int overlap_prior;                // nonzero: the previous launch is this call's chunk kernel,
                                       // which started only after its own predecessors finished;
                                       // run beside it and wait for it only before exiting
@@ -143,8 +154,8 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 
 // Decode kernels: dynamic shared memory for num_seqs sequences.
 size_t decode_smem_bytes(CacheKind kind, int num_seqs);
-cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, size_t max_smem);
-cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, size_t smem, int* ctas_per_sm);
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t max_smem);
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t smem, int* ctas_per_sm);
 cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, const DecodeParams& p, int grid, size_t smem,
                           cudaStream_t stream);

@@ -276,3 +276,37 @@ def test_mixed_rows_outside_q_are_recorded_not_faulted(bad):
     # the well-formed decode row of sequence 0 is still right
     rows, ref = oracle_step(w, seqs=[0])
     compare(out, rows, ref, "untouched decode row")
+
+
+# ------------------------------------------------ claimed pieces (dynamic tail)
+
+@pytest.mark.parametrize("workers", [4, 16, 40])
+def test_claimed_pieces_many_calls_one_workspace(workers):
+    # long ranges per worker: the last share of the blocks goes to pieces claimed from
+    # the workspace counter; consecutive calls on one workspace keep numbering them right
+    w = _case(60 + workers, [3000, 40, 1, 2500, 777, 64], 4, write_new=False)
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads)
+    rows, ref = oracle_step(w)
+    outs = []
+    for _ in range(4):
+        out, _, _ = gpu_step(w, num_workers=workers, workspace=ws)
+        compare(out, rows, ref, f"pieces, {workers} workers")
+        outs.append(out)
+    assert all(torch.equal(outs[0], o) for o in outs[1:])   # merged in slot order: reproducible
+
+
+def test_claimed_pieces_after_a_timeout_and_other_calls():
+    # a timed-out call, a plain decode and a mixed batch in between leave the counter usable
+    w = _case(64, [2000, 3000, 100], 8, write_new=False)
+    ws = pa.new_workspace(16, 64, 8)
+    pa.pa_selftest_wait_timeout(ws, 2000)
+    assert pa.pa_read_device_status(ws) == pa.PA_ERR_TIMEOUT
+    rows, ref = oracle_step(w)
+    out, _, _ = gpu_step(w, num_workers=8, workspace=ws)
+    compare(out, rows, ref, "after timeout")
+    m = _case(65, [30, 100, 64], 4, q_lens=[1, 20, 64])
+    mo, _, _ = gpu_step(m, workspace=ws)
+    mrows, mref = oracle_step(m)
+    compare(mo, mrows, mref, "mixed in between")
+    out, _, _ = gpu_step(w, num_workers=8, workspace=ws)
+    compare(out, rows, ref, "after mixed")
