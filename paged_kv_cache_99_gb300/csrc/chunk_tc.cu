@@ -472,21 +472,25 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             m_used = m_new;
             // p = 2^(s * scale - m) as the 16-bit A operand of P.V, written over the
             // columns of S (keys 32 c .. +31 -> columns 16 c .. +15)
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-            const float neg_m = -m_new;
+            // (s * scale - m) and the running sums two columns per instruction (f32x2)
+            uint64_t sum2[2] = {0ull, 0ull};
+            const uint64_t scale2 = f2_pack(s_log2, s_log2);
+            const uint64_t negm2 = f2_pack(-m_new, -m_new);
 #pragma unroll
             for (int c = 0; c < kTcKeys / 32; ++c) {
                 uint32_t pw[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const int k = 32 * c + e;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sv[k]), s_log2, neg_m));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sv[k + 1]), s_log2, neg_m));
+                    float a0, a1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), scale2, negm2), a0, a1);
+                    float p0 = ex2_approx(a0);
+                    float p1 = ex2_approx(a1);
                     if (need_mask) {
                         p0 = k <= lim ? p0 : 0.f;
                         p1 = k + 1 <= lim ? p1 : 0.f;
                     }
-                    sum4[(e >> 1) & 3] += p0 + p1;
+                    sum2[(e >> 1) & 1] = f2_add(sum2[(e >> 1) & 1], f2_pack(p0, p1));
                     pw[e >> 1] = pack2<kMmaBf16>(p0, p1);
                 }
                 tmem_st16(s_addr + 16 * c, pw);
@@ -504,7 +508,10 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 }
             }
             tmem_wait_st();
-            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            float s0, s1, s2, s3;
+            f2_unpack(sum2[0], s0, s1);
+            f2_unpack(sum2[1], s2, s3);
+            l = l * alpha + ((s0 + s1) + (s2 + s3));
             bool zeroed = false;
             if constexpr (!kFp8) {
                 // keys past the CTA's last position get P = 0, but their V rows hold unloaded
