@@ -529,16 +529,13 @@ def run_reference(args, rank, world):
     }
 
 
-def run_copy_blocks(args, rank, world, local, l2: bool = False):
+def run_copy_blocks(args, rank, world, local):
     """Copy-on-write block copies (pa_copy_blocks) on a pool shaped like one layer of the
-    40-layer GQA model (8 KV heads, fp16): `pairs` distinct src -> dst blocks per step.
-    With l2, the pool (K and V, 48 MB) stays resident in L2 and the copies measure the
-    L2's read + write rate, the ceiling of traffic that hits there (the shared prefix
-    read by every sequence)."""
+    40-layer GQA model (8 KV heads, fp16): `pairs` distinct src -> dst blocks per step."""
     import paged_kv_cache_99_gb300 as pa
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    nb, hkv, pairs = (768, 8, 384) if l2 else (40_000, 8, 16_384)
+    nb, hkv, pairs = 40_000, 8, 16_384
     g = torch.Generator(device=dev).manual_seed(1010)
     bs = args.block_size
     nb = nb * W.BLOCK_SIZE // bs                         # the same pool and copied bytes at every block size
@@ -554,41 +551,31 @@ def run_copy_blocks(args, rank, world, local, l2: bool = False):
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
-    # the L2 case copies in a captured graph of `reps` launches: a launch from the host
-    # takes longer than the copy itself
-    reps = 32 if l2 else 1
-    g_copy = capture(lambda: [pa.pa_copy_blocks(k, v, src, dst) for _ in range(reps)]) if l2 else None
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         ev[i][0].record()
-        if l2:
-            g_copy.replay()
-        else:
-            pa.pa_copy_blocks(k, v, src, dst)
+        pa.pa_copy_blocks(k, v, src, dst)
         ev[i][1].record()
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev) / args.steps / reps, world)
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world)
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     gbs = moved / (ms * 1e-3) / 1e9
     return {
-        "metric": ("L2-resident block copy GB/s (read + write bytes)" if l2 else
-                   "copy-on-write block copy GB/s (read + write bytes)"),
+        "metric": "copy-on-write block copy GB/s (read + write bytes)",
         "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
         "config": {"workload": f"copy {pairs} blocks of {hkv} KV heads x {bs} x 128 fp16 (K and V) per step, "
-                               f"pool of {nb} blocks ({2 * nb * block_bytes / 1e9:.3f} GB)",
-                   "l2": "pool resident in L2 (no flush)" if l2 else "inputs larger than L2"},
-        "roofline": {"kernel": "copy_blocks_kernel", "bound": "l2" if l2 else "hbm", "achieved": round(gbs, 2),
-                     "peak": None if l2 else hbm_peak,
-                     "peak_source": "this is the L2 measurement" if l2 else
-                                    f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, a copy)", "unit": "GB/s",
-                     "frac": None if l2 else round(gbs / hbm_peak, 4), "traffic": None,
-                     "algorithmic_bytes_per_launch": moved, "avg_launch_ms": round(ms, 5)},
-        "gpu_launches": args.steps * reps, "clocks": clk,
+                               f"pool of {nb} blocks ({2 * nb * block_bytes / 1e9:.1f} GB)",
+                   "l2": "inputs larger than L2"},
+        "roofline": {"kernel": "copy_blocks_kernel", "bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, a copy)", "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None, "algorithmic_bytes_per_launch": moved,
+                     "avg_launch_ms": round(ms, 5)},
+        "gpu_launches": args.steps, "clocks": clk,
     }
 
 
@@ -602,9 +589,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix workload through pa_decode_shared_prefix (prefix once on the tensor cores)")
-    ap.add_argument("--op", default="attention", choices=["attention", "copy-blocks", "l2-copy"],
-                    help="copy-blocks: time the copy-on-write block copies instead of the attention step; "
-                         "l2-copy: the same on a pool resident in L2 (the L2 rate)")
+    ap.add_argument("--op", default="attention", choices=["attention", "copy-blocks"],
+                    help="copy-blocks: time the copy-on-write block copies instead of the attention step")
     ap.add_argument("--block-size", type=int, default=W.BLOCK_SIZE, choices=[8, 16, 32],
                     help="tokens per cache block (the named workloads are built with 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -619,8 +605,8 @@ def main(argv=None):
         dist.init_process_group("nccl")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
-    elif args.op in ("copy-blocks", "l2-copy"):
-        line = run_copy_blocks(args, rank, world, local, l2=args.op == "l2-copy")
+    elif args.op == "copy-blocks":
+        line = run_copy_blocks(args, rank, world, local)
     else:
         line = run_ours(args, rank, world, local)
     if rank == 0 and line is not None:
