@@ -50,6 +50,8 @@ DESCRIPTIONS = {
                      "+ private suffix U[0,1000]",
     "shared-prefix-long": "shared-prefix decode, long prompt: 1 layer, B=32, H_q=32, H_kv=8, bf16, 512 aliased "
                           "prefix blocks (8192 tokens) + private suffix U[0,512]",
+    "shared-prefix-l2": "shared-prefix decode, prefix only: 1 layer, B=128, H_q=32, H_kv=8, bf16, 128 aliased "
+                        "prefix blocks and no private tokens (the decode's L2 ceiling for shared blocks)",
     "mixed-fp8": "mixed fp8: 1 layer, H_q=64, H_kv=8, e4m3 KV, 16 decode rows (lognormal median 8192, cap 32768) "
                  "+ 2 prefill chunks of 512 on 4096-token contexts",
 }

@@ -303,6 +303,13 @@ def shared_prefix_long(device, seed: int = 1006, batch: int = 32, prefix_tokens:
                          block_size=block_size)
 
 
+def shared_prefix_l2(device, seed: int = 1007, batch: int = 128, block_size: int = BLOCK_SIZE) -> Workload:
+    # every sequence is the shared 2048-token prefix and nothing else: after its first
+    # read the prefix is served from L2, so the decode's rate here is its L2 ceiling
+    # for the shared-prefix batch's logical bytes
+    return shared_prefix(device, seed=seed, batch=batch, prefix_tokens=2048, max_suffix=0, block_size=block_size)
+
+
 def mixed_fp8(device, seed: int = 1005, num_decode: int = 16, num_chunks: int = 2,
               chunk_len: int = 512, chunk_ctx: int = 4096, median: int = 8192,
               sigma: float = 1.0, cap: int = 32768, block_size: int = BLOCK_SIZE) -> Workload:
@@ -322,6 +329,7 @@ NAMED = {
     "gqa40-8k": gqa40_8k,
     "shared-prefix": shared_prefix,
     "shared-prefix-long": shared_prefix_long,
+    "shared-prefix-l2": shared_prefix_l2,
     "mixed-fp8": mixed_fp8,
 }
 
