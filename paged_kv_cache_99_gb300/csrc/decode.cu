@@ -162,6 +162,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ int warp_tot[kDecodeWarps];
+    __shared__ int staged_unit[kDecodeWarps];   // static ranges: unit whose partial a warp left here
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t tiles = (raw_base + 1023u) & ~1023u;     // 128-byte swizzle needs 1 KiB alignment
     uint8_t* aligned = smem_raw + (tiles - raw_base);
@@ -255,7 +256,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     if (T == 0) return;
     const Split sp = make_split(T, p.num_workers, p.dyn256);
     const int wid = blockIdx.x * kDecodeWarps + warp;
-    if (wid >= p.num_workers) return;
+    // With static ranges the warps of a CTA, whose ranges follow one another, merge
+    // the partials of the unit their ranges end in before one of them writes it: a
+    // unit then leaves one partial per CTA it spans, not one per warp.  Every warp
+    // reaches that merge, with or without work.
+    int my_staged = -1;
+    if (wid < p.num_workers) do {
     // pieces are numbered from the counter's value when this call began (the
     // previous call's combine set claim[1] to the counter's final value)
     const unsigned claim_base = __ldcg(p.claim + 1);
@@ -285,7 +291,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
         c_lo = static_cast<int>(static_cast<long long>(sp.Ts) * wid / sp.W);
         c_hi = static_cast<int>(static_cast<long long>(sp.Ts) * (wid + 1) / sp.W);
     } else if (!Dyn || !claim(c_lo, c_hi, c_ri)) {
-        return;
+        break;
     }
     const Cursor start = locate(c_lo, cum, B, UH);
 
@@ -486,7 +492,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
                     mbar_wait_bounded(my_bars + 8 * (k % NS), (k / NS) & 1, p.timeout_ns);
             }
             __syncwarp();
-            return;
+            break;
         }
         mbar_try_wait(bar, parity);   // phase is complete: acquire for every lane
 
@@ -663,19 +669,24 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
             const int fu = cum[C.s] + C.uh * C.nb;
             // a unit one range covers is written directly, unless a prefix partial waits for it
             const bool write = !p.cascade && sp.range_of(fu) == sp.range_of(fu + C.nb - 1);
+            // static ranges: a unit that goes on past this range's end (the range's last
+            // segment; the ring is idle) is staged in the warp's ring for the CTA merge
+            const bool stage = !Dyn && !write && C.j != C.nb - 1;
             if (!write) {
                 // unit shared with other ranges: plain partial store, merged by combine_kernel
                 const int slot = c_ri + u;
-                float4* part = p.partial + static_cast<size_t>(slot) * 8 * 32;
+                float4* part = stage ? reinterpret_cast<float4*>(aligned + warp * NS * STAGE)
+                                     : p.partial + static_cast<size_t>(slot) * 8 * 32;
 #pragma unroll
                 for (int dt = 0; dt < 8; ++dt) part[dt * 32 + lane] = make_float4(o[dt][0], o[dt][1], o[dt][2], o[dt][3]);
                 if (lane < 4) {
-                    float* ml = p.ml + static_cast<size_t>(slot) * 16;
+                    float* ml = stage ? reinterpret_cast<float*>(part + 8 * 32) : p.ml + static_cast<size_t>(slot) * 16;
                     ml[2 * t] = m0;
                     ml[2 * t + 1] = m1;
                     ml[8 + 2 * t] = l0;
                     ml[8 + 2 * t + 1] = l1;
                 }
+                if (stage) my_staged = u;
             }
             if (write) {
                 const int h = C.uh / p.head_groups;
@@ -715,6 +726,50 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
             open = false;
         } else {
             cursor_advance(C, cum, B, UH);
+        }
+    }
+    } while (false);
+
+    if constexpr (!Dyn) {
+        // ---- CTA merge of staged partials: the first warp of each run of warps that
+        // staged the same unit folds the run and writes one partial (slot wid + unit) ----
+        if (lane == 0) staged_unit[warp] = my_staged;
+        __syncthreads();
+        if (my_staged >= 0 && (warp == 0 || staged_unit[warp - 1] != my_staged)) {
+            const int t = lane & 3;
+            float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+            float4 acc[8];
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) acc[dt] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w2 = warp; w2 < kDecodeWarps && staged_unit[w2] == my_staged; ++w2) {
+                const float4* part = reinterpret_cast<const float4*>(aligned + w2 * NS * STAGE);
+                const float* ml = reinterpret_cast<const float*>(part + 8 * 32);
+                const float m0w = ml[2 * t], m1w = ml[2 * t + 1], l0w = ml[8 + 2 * t], l1w = ml[8 + 2 * t + 1];
+                const float n0 = fmaxf(M0, m0w), n1 = fmaxf(M1, m1w);
+                const float r0 = exp2f(M0 - n0), r1 = exp2f(M1 - n1);      // 0 while nothing is summed
+                const float w0 = exp2f(m0w - n0), w1 = exp2f(m1w - n1);
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    const float4 x = part[dt * 32 + lane];
+                    acc[dt] = make_float4(acc[dt].x * r0 + x.x * w0, acc[dt].y * r1 + x.y * w1,
+                                          acc[dt].z * r0 + x.z * w0, acc[dt].w * r1 + x.w * w1);
+                }
+                L0 = L0 * r0 + l0w * w0;
+                L1 = L1 * r1 + l1w * w1;
+                M0 = n0;
+                M1 = n1;
+            }
+            const int slot = wid + my_staged;
+            float4* gpart = p.partial + static_cast<size_t>(slot) * 8 * 32;
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) gpart[dt * 32 + lane] = acc[dt];
+            if (lane < 4) {
+                float* gml = p.ml + static_cast<size_t>(slot) * 16;
+                gml[2 * t] = M0;
+                gml[2 * t + 1] = M1;
+                gml[8 + 2 * t] = L0;
+                gml[8 + 2 * t + 1] = L1;
+            }
         }
     }
 }
@@ -770,14 +825,23 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
     }
     const int nb = unit_blocks_of(p, s, UH) / UH;
     const bool pre = Cascade && p.first_block > 0;     // every row has a shared-prefix partial
-    int wa = 0, nseg = 0;
+    // the unit's partials: one per range it spans (ranges wa .. wb), or with static
+    // ranges, where each CTA merged the partials of the unit its warps' ranges end in,
+    // one for wa, one for the first warp of every later CTA before wb, and one for wb
+    int wa = 0, wb = 0, nseg = 0, m0 = 0;
+    const bool cta_merged = p.dyn256 == 0;
     if (nb > 0 && T > 0) {
         const Split sp = make_split(static_cast<int>(T), p.num_workers, p.dyn256);
         const int fu = static_cast<int>(lo) + uh * nb;
         wa = sp.range_of(fu);
-        const int wb = sp.range_of(fu + nb - 1);
+        wb = sp.range_of(fu + nb - 1);
         if (wa == wb && !Cascade) return;     // its only range wrote the output
-        nseg = wb - wa + 1;
+        if (!cta_merged || wa == wb) {
+            nseg = wb - wa + 1;
+        } else {
+            m0 = (wa / kDecodeWarps + 1) * kDecodeWarps;
+            nseg = 2 + (m0 <= wb - 1 ? (wb - 1 - m0) / kDecodeWarps + 1 : 0);
+        }
     } else if (!pre) {
         return;   // an empty row: the decode grid wrote its zeros
     }
@@ -857,13 +921,18 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
             fold(v, mv, lv, min(kBatch, npre - base));
         }
     }
+    // range of the unit's k-th partial
+    auto range_k = [&](int k) -> int {
+        if (!cta_merged || wa == wb) return wa + k;
+        return k == 0 ? wa : (k == nseg - 1 ? wb : m0 + kDecodeWarps * (k - 1));
+    };
     // the decode slots of the unit's segments
     for (int base = 0; base < nseg; base += kBatch) {
         float4 v[kBatch];
         float2 mv[kBatch], lv[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
-            const int sl = wa + min(base + k, nseg - 1) + u;
+            const int sl = range_k(min(base + k, nseg - 1)) + u;
             v[k] = __ldcg(p.partial + (static_cast<size_t>(sl) * 8 + dt) * 32 + lane);
             mv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 2 * t));
             lv[k] = __ldcg(reinterpret_cast<const float2*>(p.ml + static_cast<size_t>(sl) * 16 + 8 + 2 * t));
