@@ -1094,9 +1094,12 @@ cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // slots per round trip: 8 in the cascade variant (which also folds prefix
-    // partials) and where units average under 8 segments, else 10 (at most 112
+    // partials) and where units average under 8 partials, else 10 (at most 112
     // registers either way)
-    const bool wide = !p.cascade && static_cast<long long>(p.num_workers) > 8 * units;
+    // (with static ranges a unit leaves about one partial per CTA it spans, otherwise
+    // one per range)
+    const long long per_slot = p.dyn256 == 0 ? 4LL * kDecodeWarps : 8LL;
+    const bool wide = !p.cascade && static_cast<long long>(p.num_workers) > per_slot * units;
     auto kernel = [&](auto ob, auto f8) -> const void* {
         constexpr bool O = decltype(ob)::value, F = decltype(f8)::value;
         if (p.cascade) return reinterpret_cast<const void*>(&combine_kernel<O, F, true, 8>);
