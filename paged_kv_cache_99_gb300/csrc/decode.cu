@@ -969,6 +969,9 @@ template <bool OutBf16, bool Fp8Layout, bool Cascade, int kBatch>
 __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
     __shared__ int pre_sum[kCombineScanSeqs + 1];
     __shared__ int warp_sum[8];
+    // a launch chained behind (the next layer's decode) may become resident now and
+    // wait for this grid's completion with its prologue done
+    grid_launch_dependents();
     const int B = p.num_seqs;
     const int UH = p.num_kv_heads * p.head_groups;
     if (B <= kCombineScanSeqs) {
