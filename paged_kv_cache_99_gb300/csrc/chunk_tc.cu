@@ -43,31 +43,32 @@ namespace {
 
 constexpr int kTcRows = 128;                 // MMA M of one tile
 constexpr int kTcKeys = 128;                 // keys per step (MMA N of S, K of P.V)
-constexpr int kTcStages = 2;
+constexpr int kKStages = 2;                  // K ring (its copies run a step ahead of V's)
+constexpr int kVStages = 2;                  // V ring
 constexpr uint32_t kQHalf = 16384;           // Q tile: [128 rows][64 elements] per d-half
 constexpr uint32_t kKvHalf = 16384;          // K or V of a step: [128 keys][64 elements] per d-half
 constexpr uint32_t kKvBytes = 2 * kKvHalf;
 constexpr uint32_t kOffQ = 0;                // Q_A, Q_B: 32 KiB each
 constexpr uint32_t kOffK = 65536;            // K stages, 32 KiB each
-constexpr uint32_t kOffV = kOffK + kTcStages * kKvBytes;      // V stages, 32 KiB each
-constexpr uint32_t kOffBars = kOffV + kTcStages * kKvBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kKvBytes;       // V stages, 32 KiB each
+constexpr uint32_t kOffBars = kOffV + kVStages * kKvBytes;
 constexpr uint32_t kBarBytes = 256;          // barriers + tensor-memory address
-constexpr uint32_t kOffCum = kOffBars + kBarBytes;
 constexpr uint32_t kTmemCols = 512;          // S_A/P_A 0  S_B/P_B 128  O_A 256  O_B 384
 constexpr float kRescaleLog2 = 8.0f;         // lazy rescale threshold (factor 256)
 
 // barrier indices (8 bytes each from kOffBars)
 enum {
-    kBarKFull = 0,      // [stage]
-    kBarKEmpty = 2,     // [stage]
-    kBarVFull = 4,      // [stage]
-    kBarVEmpty = 6,     // [stage]
-    kBarSFull = 8,      // [tile]
-    kBarPFull = 10,     // [tile]
-    kBarPvDone = 12,    // [tile]
-    kBarQFull = 14,
-    kNumBars = 15
+    kBarKFull = 0,                          // [K stage]
+    kBarKEmpty = kBarKFull + kKStages,      // [K stage]
+    kBarVFull = kBarKEmpty + kKStages,      // [V stage]
+    kBarVEmpty = kBarVFull + kVStages,      // [V stage]
+    kBarSFull = kBarVEmpty + kVStages,      // [tile]
+    kBarPFull = kBarSFull + 2,              // [tile]
+    kBarPvDone = kBarPFull + 2,             // [tile]
+    kBarQFull = kBarPvDone + 2,
+    kNumBars = kBarQFull + 1
 };
+static_assert(kNumBars * 8 + 4 <= kBarBytes, "barriers");
 
 template <int Kind>
 struct TcCfg {
@@ -121,20 +122,22 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ int warp_tot[Cfg::kWarps];
+    __shared__ int pick[2];                  // this CTA's chunk sequence and tile pair
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (sbase - raw_base);
-    int* cum = reinterpret_cast<int*>(sm + kOffCum);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBars + kNumBars * 8);
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8u * i; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(kBarKFull + s), kFp8 ? 2 : 1);
-            mbar_init(bar(kBarVFull + s), kFp8 ? 2 : 1);
             mbar_init(bar(kBarKEmpty + s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(bar(kBarVFull + s), kFp8 ? 2 : 1);
             mbar_init(bar(kBarVEmpty + s), 1);
         }
         for (int x = 0; x < 2; ++x) {
@@ -157,7 +160,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     const bool prefix = p.prefix_keys > 0;
     int s = 0, pair = 0, q0 = 0, q_len = 0, n = 0;
     if (!prefix) {
-        // ---- tile pairs per chunk sequence, exclusive scan -> cum ----
+        // ---- tile pairs per chunk sequence: exclusive scan over contiguous runs of
+        // sequences per thread; the thread whose run holds this CTA's pair names it ----
         auto pairs_of = [&](int sq) -> int {
             const int ql = p.query_start_loc[sq + 1] - p.query_start_loc[sq];
             return ql >= 2 ? (ql + 2 * QT - 1) / (2 * QT) : 0;
@@ -176,29 +180,31 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             }
             if (lane == 31) warp_tot[warp] = incl;
             __syncthreads();
-            int run = incl - local;
-            for (int w = 0; w < warp; ++w) run += warp_tot[w];
-            for (int sq = beg; sq < end; ++sq) {
-                cum[sq] = run;
-                run += pairs_of(sq);
+            int run = incl - local, total = 0;
+            for (int w = 0; w < Cfg::kWarps; ++w) {
+                run += w < warp ? warp_tot[w] : 0;
+                total += warp_tot[w];
             }
-            if (threadIdx.x == kThreads - 1) cum[B] = run;
+            const int tau = total - 1 - static_cast<int>(blockIdx.x);   // heaviest pairs first
+            if (tau >= run && tau < run + local) {
+                for (int sq = beg; sq < end; ++sq) {
+                    const int np = pairs_of(sq);
+                    if (tau < run + np) {
+                        pick[0] = sq;
+                        pick[1] = tau - run;
+                        break;
+                    }
+                    run += np;
+                }
+            }
+            if (tau < 0) pick[0] = -1;          // every thread agrees: no pair for this CTA
         }
         __syncthreads();
         grid_launch_dependents();
 
-        const int R = cum[B];
-        if (static_cast<int>(blockIdx.x) >= R) return;
-        const int tau = R - 1 - static_cast<int>(blockIdx.x);   // heaviest pairs first
-        {
-            int lo = 0, hi = B;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (cum[mid] <= tau) lo = mid; else hi = mid;
-            }
-            s = lo;
-        }
-        pair = tau - cum[s];
+        s = pick[0];
+        if (s < 0) return;
+        pair = pick[1];
         q0 = p.query_start_loc[s];
         q_len = p.query_start_loc[s + 1] - q0;
         n = p.seq_lens[s];
@@ -286,23 +292,30 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     tma_load_2d(dst + kKvHalf + (lane << rsh) * 128, map, 64, y, full);
                 }
             };
-            int y = entry(0);
+            // order K(0), K(1), V(0), K(2), V(1), ...: each K a step ahead of its V
+            auto pieces = [&](int i) { return min(per_step, npieces - (step0 + i) * per_step); };
+            int y_v = entry(0);
+            if (nsteps > 0) copy(&kmap, sbase + kOffK, bar(kBarKFull), pieces(0), y_v);
+            int y_k = nsteps > 1 ? entry(1) : 0;
             for (int i = 0; i < nsteps && ok; ++i) {
-                const int st = i % kTcStages;
-                const uint32_t par = ((i / kTcStages) - 1) & 1;
-                const int y_next = i + 1 < nsteps ? entry(i + 1) : 0;
-                const int nb = min(per_step, npieces - (step0 + i) * per_step);
-                if (i >= kTcStages && !warp_wait(bar(kBarKEmpty + st), par, p.timeout_ns)) {
+                const int y_after = i + 2 < nsteps ? entry(i + 2) : 0;
+                const int ik = i + 1;
+                if (ik < nsteps) {
+                    const int st = ik % kKStages;
+                    if (ik >= kKStages && !warp_wait(bar(kBarKEmpty + st), ((ik / kKStages) - 1) & 1, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    copy(&kmap, sbase + kOffK + st * kKvBytes, bar(kBarKFull + st), pieces(ik), y_k);
+                }
+                const int st = i % kVStages;
+                if (i >= kVStages && !warp_wait(bar(kBarVEmpty + st), ((i / kVStages) - 1) & 1, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                copy(&kmap, sbase + kOffK + st * kKvBytes, bar(kBarKFull + st), nb, y);
-                if (i >= kTcStages && !warp_wait(bar(kBarVEmpty + st), par, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                copy(&vmap, sbase + kOffV + st * kKvBytes, bar(kBarVFull + st), nb, y);
-                y = y_next;
+                copy(&vmap, sbase + kOffV + st * kKvBytes, bar(kBarVFull + st), pieces(i), y_v);
+                y_v = y_k;
+                y_k = y_after;
             }
             if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
         }
@@ -313,7 +326,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             constexpr uint32_t idPV = umma_idesc_f16<kMmaBf16>(kTcRows, kHeadDim, true);
             auto issue_s = [&](int x, int i) {
                 const uint32_t qbase = sbase + kOffQ + x * 2 * kQHalf;
-                const uint32_t kbase = sbase + kOffK + (i % kTcStages) * kKvBytes;
+                const uint32_t kbase = sbase + kOffK + (i % kKStages) * kKvBytes;
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint64_t a = umma_desc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 umma_commit(bar(kBarSFull + x));
             };
             auto issue_pv = [&](int x, int j) {
-                const uint32_t vbase = sbase + kOffV + (j % kTcStages) * kKvBytes;
+                const uint32_t vbase = sbase + kOffV + (j % kVStages) * kKvBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     // V is MN-major: d-halves kKvHalf apart, 16 keys = 2 KiB
@@ -346,7 +359,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     const int other = 1 - x;
                     const int j = next_pv[x];
                     if (j < tile_steps(x) && j < next_s[x] && mbar_test(bar(kBarPFull + x), j & 1) &&
-                        mbar_test(bar(kBarVFull + j % kTcStages), (j / kTcStages) & 1)) {
+                        mbar_test(bar(kBarVFull + j % kVStages), (j / kVStages) & 1)) {
                         // a 16-bit cache's last step also waits for the zeroing tile
                         const int pv_zt = zt ? next_pv[1] : next_pv[0];
                         const bool blocked = !kFp8 && j == nsteps - 1 && x != zt && j < tile_steps(zt) &&
@@ -357,20 +370,20 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                             next_pv[x] = j + 1;
                             progress = true;
                             if (j >= tile_steps(other) || next_pv[other] > j)
-                                umma_commit(bar(kBarVEmpty + j % kTcStages));   // both tiles done with V_j
+                                umma_commit(bar(kBarVEmpty + j % kVStages));   // both tiles done with V_j
                             if (j + 1 == tile_steps(x)) umma_commit(bar(kBarPvDone + x));
                         }
                     }
                     // this tile's next S right behind its P.V, ahead of the other tile's work
                     const int i = next_s[x];
                     if (i < tile_steps(x) && next_pv[x] >= i &&
-                        mbar_test(bar(kBarKFull + i % kTcStages), (i / kTcStages) & 1)) {
+                        mbar_test(bar(kBarKFull + i % kKStages), (i / kKStages) & 1)) {
                         tc_fence_after();
                         issue_s(x, i);
                         next_s[x] = i + 1;
                         progress = true;
                         if (i >= tile_steps(other) || next_s[other] > i)
-                            umma_commit(bar(kBarKEmpty + i % kTcStages));       // both tiles done with K_i
+                            umma_commit(bar(kBarKEmpty + i % kKStages));       // both tiles done with K_i
                     }
                 }
                 if (progress) {
@@ -517,8 +530,8 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 // keys past the CTA's last position get P = 0, but their V rows hold unloaded
                 // (stale) or poisoned bytes and 0 x NaN is NaN: the last tile zeroes them
                 if (i == nsteps - 1 && x == (has_b ? 1 : 0)) {
-                    const int st = i % kTcStages;
-                    if (!warp_wait(bar(kBarVFull + st), (i / kTcStages) & 1, p.timeout_ns)) {
+                    const int st = i % kVStages;
+                    if (!warp_wait(bar(kBarVFull + st), (i / kVStages) & 1, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -636,32 +649,31 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         load_item(kc, 0, 0, xa);
         load_item(kc, 0, 1, xb);
         for (int i = 0; i < nsteps && ok; ++i) {
-            const int st = i % kTcStages;
-            const uint32_t par = ((i / kTcStages) - 1) & 1;
-            if (i >= kTcStages && !warp_wait(bar(kBarKEmpty + st), par, p.timeout_ns)) {
+            const int sk = i % kKStages, sv = i % kVStages;
+            if (i >= kKStages && !warp_wait(bar(kBarKEmpty + sk), ((i / kKStages) - 1) & 1, p.timeout_ns)) {
                 ok = false;
                 break;
             }
-            uint8_t* kdst = sm + kOffK + st * kKvBytes;
+            uint8_t* kdst = sm + kOffK + sk * kKvBytes;
             widen_store(kdst, 0, xa);
             load_item(vc, i, 0, xa);
             widen_store(kdst, 1, xb);
             load_item(vc, i, 1, xb);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarKFull + st));
-            if (i >= kTcStages && !warp_wait(bar(kBarVEmpty + st), par, p.timeout_ns)) {
+            if (lane == 0) mbar_arrive(bar(kBarKFull + sk));
+            if (i >= kVStages && !warp_wait(bar(kBarVEmpty + sv), ((i / kVStages) - 1) & 1, p.timeout_ns)) {
                 ok = false;
                 break;
             }
-            uint8_t* vdst = sm + kOffV + st * kKvBytes;
+            uint8_t* vdst = sm + kOffV + sv * kKvBytes;
             widen_store(vdst, 0, xa);
             load_item(kc, i + 1, 0, xa);
             widen_store(vdst, 1, xb);
             load_item(kc, i + 1, 1, xb);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarVFull + st));
+            if (lane == 0) mbar_arrive(bar(kBarVFull + sv));
         }
         if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
     }
@@ -692,8 +704,8 @@ void* chunk_tc_fn(CacheKind kind, bool q_bf16) {
 }
 }  // namespace
 
-size_t chunk_smem_bytes(CacheKind, int num_seqs) {
-    return 1024 + kOffCum + static_cast<size_t>(num_seqs + 1) * 4;
+size_t chunk_smem_bytes(CacheKind, int) {
+    return 1024 + kOffBars + kBarBytes;
 }
 
 int chunk_rows() { return kTcRows; }
