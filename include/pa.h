@@ -20,7 +20,9 @@
  *           stream).  pa_stream_t is the same handle as cudaStream_t.
  * Errors.   Host-checkable problems are reported before anything is launched:
  *           PA_ERR_INVALID_ARG (null pointer, negative count, misaligned buffer,
- *           H_q not a multiple of H_kv, ...), PA_ERR_UNSUPPORTED (head_dim != 128,
+ *           H_q not a multiple of H_kv, ...; the per-sequence or per-token arrays
+ *           of an empty batch may be null: such a call does nothing and returns
+ *           PA_OK), PA_ERR_UNSUPPORTED (head_dim != 128,
  *           block_size not 8, 16 or 32, dtype pair not listed), PA_ERR_WORKSPACE (workspace
  *           too small).  A failed launch returns PA_ERR_CUDA.  Problems only the
  *           device can see (a block-table entry outside the pool, a bounded wait

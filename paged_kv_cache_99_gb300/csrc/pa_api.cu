@@ -143,7 +143,9 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
     if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (num_blocks <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace) return PA_ERR_INVALID_ARG;
+    if (!k_cache || !v_cache || !workspace) return PA_ERR_INVALID_ARG;
+    // the per-sequence arrays of an empty batch may be empty (null)
+    if (num_seqs > 0 && (!out || !q || !block_tables || !seq_lens)) return PA_ERR_INVALID_ARG;
     if (is_fp8(cache_dtype) && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(workspace, 256))
@@ -608,7 +610,7 @@ pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, con
                                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                                        scale, q_dtype, cache_dtype, k_scale, v_scale, workspace);
     if (s != PA_OK) return s;
-    if (!query_start_loc || total_q < 0 || max_q_len < 0) return PA_ERR_INVALID_ARG;
+    if ((num_seqs > 0 && !query_start_loc) || total_q < 0 || max_q_len < 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_q == 0) return PA_OK;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const bool chunks = max_q_len >= 2;

@@ -68,6 +68,19 @@ def test_decode_host_checks(lib):
     assert _decode(lib, cd=1) == 2                         # bf16 q with fp16 cache
     assert _decode(lib, scale=ctypes.c_float(float("nan"))) == 1
     assert _decode(lib, ws=ctypes.c_void_p(0x10010)) == 1  # workspace not 256-byte aligned
+    assert _decode(lib, kc=None) == 1                      # the cache is needed even for an empty batch
+
+
+def test_empty_batch_is_a_no_op(lib):
+    # B = 0: the per-sequence arrays may be null, nothing is launched
+    assert _decode(lib, B=0, out=None, q=None, bt=None, sl=None) == 0
+    assert _decode(lib, B=0, kc=None) == 1
+    f = lib.pa_mixed
+    f.argtypes = None
+    assert f(None, None, None, FAKE, FAKE, None, 4, None, 0, 0, 0, 8, 2, 128, 16, 10, ctypes.c_float(0.088), 0, 0,
+             None, None, FAKE, ctypes.c_size_t(1 << 20), None) == 0
+    assert f(None, None, None, FAKE, FAKE, None, 4, None, 2, 3, 2, 8, 2, 128, 16, 10, ctypes.c_float(0.088), 0, 0,
+             None, None, FAKE, ctypes.c_size_t(1 << 20), None) == 1   # B = 2 needs its arrays
 
 
 def test_reshape_host_checks(lib):
