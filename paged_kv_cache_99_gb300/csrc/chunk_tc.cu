@@ -55,6 +55,18 @@ constexpr uint32_t kOffBars = kOffV + kVStages * kKvBytes;
 constexpr uint32_t kBarBytes = 256;          // barriers + tensor-memory address
 constexpr uint32_t kTmemCols = 512;          // S_A/P_A 0  S_B/P_B 128  O_A 256  O_B 384
 constexpr float kRescaleLog2 = 8.0f;         // lazy rescale threshold (factor 256)
+constexpr int kRegsFront = 104;              // registers per thread of warps 0-3 after the split
+constexpr int kRegsSoftmax = 200;            // ... and of the softmax warps 4-11
+static_assert(128 * kRegsFront + 256 * kRegsSoftmax <= 384 * 168, "register split above the launch total");
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // barrier indices (8 bytes each from kOffBars)
 enum {
@@ -74,7 +86,11 @@ template <int Kind>
 struct TcCfg {
     static constexpr bool kFp8 = Kind == kKindFp8;
     static constexpr bool kMmaBf16 = Kind == kKindBf16;
-    static constexpr int kWarps = kFp8 ? 11 : 10;
+    // warp 0: TMA producer (16-bit caches); 1: MMA issuer; 2-3: FP8 converters;
+    // 4-7: softmax of tile A; 8-11: softmax of tile B.  Three warps share each
+    // sub-partition's registers, which caps a thread at 168 at launch; the first
+    // warpgroup then hands registers to the two softmax warpgroups.
+    static constexpr int kWarps = 12;
 };
 
 // Bounded wait by lane 0 of the warp, then an acquire by every lane.
@@ -260,146 +276,226 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
     auto tO = [&](int x) -> uint32_t { return tmem + 256u + 128u * x; };
     bool ok = true;
 
-    if (!kFp8 && warp == 0) {
-        // ================= producer (16-bit caches) =================
-        // A step's keys arrive as pieces of R = min(block size, 16) rows, one per lane:
-        // piece c of the step holds keys c R .. c R + R - 1, read from table entry
-        // key / bs at row key mod bs, and lands in rows c R.. of each d-half.
-        {
-            const int bsh = p.block_shift;
-            const int rsh = min(bsh, 4);                          // log2(R)
-            const int per_step = kTcKeys >> rsh;                  // pieces per step: 8 or 16
-            const int npieces = (pos_last_cta >> rsh) + 1;        // pieces up to the CTA's last key
-            auto entry = [&](int i) -> int {
-                const int c = (step0 + i) * per_step + lane;
-                int y = 0;
-                if (lane < per_step && c < npieces) {
-                    const int key = c << rsh;
-                    int phys = __ldg(bt + (key >> bsh));
+    // 384 threads x 168 registers at launch = 128 x kRegsFront + 256 x kRegsSoftmax:
+    // each warpgroup changes its share before it branches into its roles
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsFront>();
+        if (!kFp8 && warp == 0) {
+            // ================= producer (16-bit caches) =================
+            // A step's keys arrive as pieces of R = min(block size, 16) rows, one per lane:
+            // piece c of the step holds keys c R .. c R + R - 1, read from table entry
+            // key / bs at row key mod bs, and lands in rows c R.. of each d-half.
+            {
+                const int bsh = p.block_shift;
+                const int rsh = min(bsh, 4);                          // log2(R)
+                const int per_step = kTcKeys >> rsh;                  // pieces per step: 8 or 16
+                const int npieces = (pos_last_cta >> rsh) + 1;        // pieces up to the CTA's last key
+                auto entry = [&](int i) -> int {
+                    const int c = (step0 + i) * per_step + lane;
+                    int y = 0;
+                    if (lane < per_step && c < npieces) {
+                        const int key = c << rsh;
+                        int phys = __ldg(bt + (key >> bsh));
+                        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+                            atomicOr(p.status, kDevErrRange);
+                            phys = 0;
+                        }
+                        y = ((phys * p.num_kv_heads + h) << bsh) + (key & (p.block_size - 1));
+                    }
+                    return y;
+                };
+                auto copy = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int np, int y) {
+                    if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(np) * 2 * (128u << rsh));
+                    __syncwarp();
+                    if (lane < np) {
+                        tma_load_2d(dst + (lane << rsh) * 128, map, 0, y, full);
+                        tma_load_2d(dst + kKvHalf + (lane << rsh) * 128, map, 64, y, full);
+                    }
+                };
+                // order K(0), K(1), V(0), K(2), V(1), ...: each K a step ahead of its V
+                auto pieces = [&](int i) { return min(per_step, npieces - (step0 + i) * per_step); };
+                int y_v = entry(0);
+                if (nsteps > 0) copy(&kmap, sbase + kOffK, bar(kBarKFull), pieces(0), y_v);
+                int y_k = nsteps > 1 ? entry(1) : 0;
+                for (int i = 0; i < nsteps && ok; ++i) {
+                    const int y_after = i + 2 < nsteps ? entry(i + 2) : 0;
+                    const int ik = i + 1;
+                    if (ik < nsteps) {
+                        const int st = ik % kKStages;
+                        if (ik >= kKStages && !warp_wait(bar(kBarKEmpty + st), ((ik / kKStages) - 1) & 1, p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        copy(&kmap, sbase + kOffK + st * kKvBytes, bar(kBarKFull + st), pieces(ik), y_k);
+                    }
+                    const int st = i % kVStages;
+                    if (i >= kVStages && !warp_wait(bar(kBarVEmpty + st), ((i / kVStages) - 1) & 1, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    copy(&vmap, sbase + kOffV + st * kKvBytes, bar(kBarVFull + st), pieces(i), y_v);
+                    y_v = y_k;
+                    y_k = y_after;
+                }
+                if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
+            }
+        } else if (warp == 1) {
+            // ================= MMA issuer =================
+            if (lane == 0) {
+                constexpr uint32_t idS = umma_idesc_f16<kMmaBf16>(kTcRows, kTcKeys, false);
+                constexpr uint32_t idPV = umma_idesc_f16<kMmaBf16>(kTcRows, kHeadDim, true);
+                auto issue_s = [&](int x, int i) {
+                    const uint32_t qbase = sbase + kOffQ + x * 2 * kQHalf;
+                    const uint32_t kbase = sbase + kOffK + (i % kKStages) * kKvBytes;
+    #pragma unroll
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                        const uint64_t a = umma_desc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = umma_desc_sw128(kbase + (kk >> 2) * kKvHalf + (kk & 3) * 32, 16, 1024);
+                        umma_f16(tS(x), a, b, idS, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(kBarSFull + x));
+                };
+                auto issue_pv = [&](int x, int j) {
+                    const uint32_t vbase = sbase + kOffV + (j % kVStages) * kKvBytes;
+    #pragma unroll
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                        // V is MN-major: d-halves kKvHalf apart, 16 keys = 2 KiB
+                        const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
+                        umma_f16_ts(tO(x), tS(x) + 8 * kk, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                };
+                // Event loop: poll the barriers and issue whatever is ready, P.V first (the
+                // next S of that tile waits for it), then S.  No barrier tested here can run
+                // a phase ahead: each one's next phase needs an MMA not yet issued.
+                const int zt = has_b ? 1 : 0;             // tile that zeroes V rows in the last step
+                int next_s[2] = {0, 0}, next_pv[2] = {0, 0};
+                ok = mbar_wait_bounded(bar(kBarQFull), 0, p.timeout_ns);
+                uint64_t t_last = 0;
+                uint32_t idle = 0;
+                while (ok && (next_pv[0] < tile_steps(0) || next_pv[1] < tile_steps(1))) {
+                    bool progress = false;
+    #pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const int other = 1 - x;
+                        const int j = next_pv[x];
+                        if (j < tile_steps(x) && j < next_s[x] && mbar_test(bar(kBarPFull + x), j & 1) &&
+                            mbar_test(bar(kBarVFull + j % kVStages), (j / kVStages) & 1)) {
+                            // a 16-bit cache's last step also waits for the zeroing tile
+                            const int pv_zt = zt ? next_pv[1] : next_pv[0];
+                            const bool blocked = !kFp8 && j == nsteps - 1 && x != zt && j < tile_steps(zt) &&
+                                                 !(pv_zt > j || mbar_test(bar(kBarPFull + zt), j & 1));
+                            if (!blocked) {
+                                tc_fence_after();
+                                issue_pv(x, j);
+                                next_pv[x] = j + 1;
+                                progress = true;
+                                if (j >= tile_steps(other) || next_pv[other] > j)
+                                    umma_commit(bar(kBarVEmpty + j % kVStages));   // both tiles done with V_j
+                                if (j + 1 == tile_steps(x)) umma_commit(bar(kBarPvDone + x));
+                            }
+                        }
+                        // this tile's next S right behind its P.V, ahead of the other tile's work
+                        const int i = next_s[x];
+                        if (i < tile_steps(x) && next_pv[x] >= i &&
+                            mbar_test(bar(kBarKFull + i % kKStages), (i / kKStages) & 1)) {
+                            tc_fence_after();
+                            issue_s(x, i);
+                            next_s[x] = i + 1;
+                            progress = true;
+                            if (i >= tile_steps(other) || next_s[other] > i)
+                                umma_commit(bar(kBarKEmpty + i % kKStages));       // both tiles done with K_i
+                        }
+                    }
+                    if (progress) {
+                        idle = 0;
+                    } else if (++idle == 1) {
+                        t_last = global_timer_ns();
+                    } else if ((idle & 255) == 0 && global_timer_ns() - t_last > p.timeout_ns) {
+                        ok = false;
+                    }
+                }
+                if (!ok) atomicOr(p.status, kDevErrTimeout);
+            }
+            __syncwarp();
+        } else if (kFp8 && (warp == 2 || warp == 3)) {
+            // ================= FP8 converters: warps 2 and 3 =================
+            // A step's K (and its V) is two items of 64 keys; thread = one key row (128 d)
+            // of an item.  Items are fetched two ahead, in the order K(i) 0, K(i) 1,
+            // V(i) 0, V(i) 1, K(i+1) 0, ...
+            const int krow = warp == 2 ? lane : 32 + lane;     // key within the item
+            auto load_item = [&](const uint8_t* cache, int i, int u, uint4 (&x8)[8]) {
+                const int key = (step0 + i) * kTcKeys + 64 * u + krow;
+                if (i < nsteps && key <= pos_last_cta) {      // later keys get P = 0: store zeros
+                    int phys = __ldg(bt + (key >> p.block_shift));
                     if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
                         atomicOr(p.status, kDevErrRange);
                         phys = 0;
                     }
-                    y = ((phys * p.num_kv_heads + h) << bsh) + (key & (p.block_size - 1));
-                }
-                return y;
-            };
-            auto copy = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int np, int y) {
-                if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(np) * 2 * (128u << rsh));
-                __syncwarp();
-                if (lane < np) {
-                    tma_load_2d(dst + (lane << rsh) * 128, map, 0, y, full);
-                    tma_load_2d(dst + kKvHalf + (lane << rsh) * 128, map, 64, y, full);
+                    const size_t off = (((static_cast<size_t>(phys) * p.num_kv_heads + h) << p.block_shift) +
+                                        (key & (p.block_size - 1))) * kHeadDim;
+                    const uint4* src = reinterpret_cast<const uint4*>(cache + off);
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) x8[e] = __ldg(src + e);
+                } else {
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) x8[e] = make_uint4(0, 0, 0, 0);
                 }
             };
-            // order K(0), K(1), V(0), K(2), V(1), ...: each K a step ahead of its V
-            auto pieces = [&](int i) { return min(per_step, npieces - (step0 + i) * per_step); };
-            int y_v = entry(0);
-            if (nsteps > 0) copy(&kmap, sbase + kOffK, bar(kBarKFull), pieces(0), y_v);
-            int y_k = nsteps > 1 ? entry(1) : 0;
-            for (int i = 0; i < nsteps && ok; ++i) {
-                const int y_after = i + 2 < nsteps ? entry(i + 2) : 0;
-                const int ik = i + 1;
-                if (ik < nsteps) {
-                    const int st = ik % kKStages;
-                    if (ik >= kKStages && !warp_wait(bar(kBarKEmpty + st), ((ik / kKStages) - 1) & 1, p.timeout_ns)) {
-                        ok = false;
-                        break;
+            auto widen_store = [&](uint8_t* stage, int u, const uint4 (&x8)[8]) {
+                // 128 e4m3 codes -> exact f16, two d-halves, 128-byte swizzle
+                const int row = 64 * u + krow;
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t w[4] = {x8[e].x, x8[e].y, x8[e].z, x8[e].w};
+                    uint32_t f[8];
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        f[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
+                        f[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
                     }
-                    copy(&kmap, sbase + kOffK + st * kKvBytes, bar(kBarKFull + st), pieces(ik), y_k);
+                    uint8_t* dst = stage + (e >> 2) * kKvHalf;
+                    *reinterpret_cast<uint4*>(dst + sw128_offset(row, 16 * (e & 3))) = make_uint4(f[0], f[1], f[2], f[3]);
+                    *reinterpret_cast<uint4*>(dst + sw128_offset(row, 16 * (e & 3) + 8)) = make_uint4(f[4], f[5], f[6], f[7]);
                 }
-                const int st = i % kVStages;
-                if (i >= kVStages && !warp_wait(bar(kBarVEmpty + st), ((i / kVStages) - 1) & 1, p.timeout_ns)) {
+            };
+            const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
+            const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
+            uint4 xa[8], xb[8];
+            load_item(kc, 0, 0, xa);
+            load_item(kc, 0, 1, xb);
+            for (int i = 0; i < nsteps && ok; ++i) {
+                const int sk = i % kKStages, sv = i % kVStages;
+                if (i >= kKStages && !warp_wait(bar(kBarKEmpty + sk), ((i / kKStages) - 1) & 1, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                copy(&vmap, sbase + kOffV + st * kKvBytes, bar(kBarVFull + st), pieces(i), y_v);
-                y_v = y_k;
-                y_k = y_after;
+                uint8_t* kdst = sm + kOffK + sk * kKvBytes;
+                widen_store(kdst, 0, xa);
+                load_item(vc, i, 0, xa);
+                widen_store(kdst, 1, xb);
+                load_item(vc, i, 1, xb);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarKFull + sk));
+                if (i >= kVStages && !warp_wait(bar(kBarVEmpty + sv), ((i / kVStages) - 1) & 1, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* vdst = sm + kOffV + sv * kKvBytes;
+                widen_store(vdst, 0, xa);
+                load_item(kc, i + 1, 0, xa);
+                widen_store(vdst, 1, xb);
+                load_item(kc, i + 1, 1, xb);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarVFull + sv));
             }
             if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
         }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
-            constexpr uint32_t idS = umma_idesc_f16<kMmaBf16>(kTcRows, kTcKeys, false);
-            constexpr uint32_t idPV = umma_idesc_f16<kMmaBf16>(kTcRows, kHeadDim, true);
-            auto issue_s = [&](int x, int i) {
-                const uint32_t qbase = sbase + kOffQ + x * 2 * kQHalf;
-                const uint32_t kbase = sbase + kOffK + (i % kKStages) * kKvBytes;
-#pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    const uint64_t a = umma_desc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = umma_desc_sw128(kbase + (kk >> 2) * kKvHalf + (kk & 3) * 32, 16, 1024);
-                    umma_f16(tS(x), a, b, idS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(bar(kBarSFull + x));
-            };
-            auto issue_pv = [&](int x, int j) {
-                const uint32_t vbase = sbase + kOffV + (j % kVStages) * kKvBytes;
-#pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    // V is MN-major: d-halves kKvHalf apart, 16 keys = 2 KiB
-                    const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
-                    umma_f16_ts(tO(x), tS(x) + 8 * kk, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-            };
-            // Event loop: poll the barriers and issue whatever is ready, P.V first (the
-            // next S of that tile waits for it), then S.  No barrier tested here can run
-            // a phase ahead: each one's next phase needs an MMA not yet issued.
-            const int zt = has_b ? 1 : 0;             // tile that zeroes V rows in the last step
-            int next_s[2] = {0, 0}, next_pv[2] = {0, 0};
-            ok = mbar_wait_bounded(bar(kBarQFull), 0, p.timeout_ns);
-            uint64_t t_last = 0;
-            uint32_t idle = 0;
-            while (ok && (next_pv[0] < tile_steps(0) || next_pv[1] < tile_steps(1))) {
-                bool progress = false;
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int other = 1 - x;
-                    const int j = next_pv[x];
-                    if (j < tile_steps(x) && j < next_s[x] && mbar_test(bar(kBarPFull + x), j & 1) &&
-                        mbar_test(bar(kBarVFull + j % kVStages), (j / kVStages) & 1)) {
-                        // a 16-bit cache's last step also waits for the zeroing tile
-                        const int pv_zt = zt ? next_pv[1] : next_pv[0];
-                        const bool blocked = !kFp8 && j == nsteps - 1 && x != zt && j < tile_steps(zt) &&
-                                             !(pv_zt > j || mbar_test(bar(kBarPFull + zt), j & 1));
-                        if (!blocked) {
-                            tc_fence_after();
-                            issue_pv(x, j);
-                            next_pv[x] = j + 1;
-                            progress = true;
-                            if (j >= tile_steps(other) || next_pv[other] > j)
-                                umma_commit(bar(kBarVEmpty + j % kVStages));   // both tiles done with V_j
-                            if (j + 1 == tile_steps(x)) umma_commit(bar(kBarPvDone + x));
-                        }
-                    }
-                    // this tile's next S right behind its P.V, ahead of the other tile's work
-                    const int i = next_s[x];
-                    if (i < tile_steps(x) && next_pv[x] >= i &&
-                        mbar_test(bar(kBarKFull + i % kKStages), (i / kKStages) & 1)) {
-                        tc_fence_after();
-                        issue_s(x, i);
-                        next_s[x] = i + 1;
-                        progress = true;
-                        if (i >= tile_steps(other) || next_s[other] > i)
-                            umma_commit(bar(kBarKEmpty + i % kKStages));       // both tiles done with K_i
-                    }
-                }
-                if (progress) {
-                    idle = 0;
-                } else if (++idle == 1) {
-                    t_last = global_timer_ns();
-                } else if ((idle & 255) == 0 && global_timer_ns() - t_last > p.timeout_ns) {
-                    ok = false;
-                }
-            }
-            if (!ok) atomicOr(p.status, kDevErrTimeout);
-        }
-        __syncwarp();
-    } else if (warp >= 2 && warp < 10) {
-        // ================= softmax: warps 2-5 tile A, 6-9 tile B; thread = one MMA row =================
-        const int x = warp < 6 ? 0 : 1;
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
+        // ================= softmax: warps 4-7 tile A, 8-11 tile B; thread = one MMA row =================
+        const int x = warp < 8 ? 0 : 1;
         const int quarter = warp & 3;                  // tensor-memory lanes 32 quarter .. + 31
         const int r = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -602,80 +698,6 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 atomicOr(p.status, kDevErrTimeout);
             }
         }
-    } else if constexpr (kFp8) {
-        // ================= FP8 converters: warps 0 and 10 =================
-        // A step's K (and its V) is two items of 64 keys; thread = one key row (128 d)
-        // of an item.  Items are fetched two ahead, in the order K(i) 0, K(i) 1,
-        // V(i) 0, V(i) 1, K(i+1) 0, ...
-        const int krow = warp == 0 ? lane : 32 + lane;     // key within the item
-        auto load_item = [&](const uint8_t* cache, int i, int u, uint4 (&x8)[8]) {
-            const int key = (step0 + i) * kTcKeys + 64 * u + krow;
-            if (i < nsteps && key <= pos_last_cta) {      // later keys get P = 0: store zeros
-                int phys = __ldg(bt + (key >> p.block_shift));
-                if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
-                    atomicOr(p.status, kDevErrRange);
-                    phys = 0;
-                }
-                const size_t off = (((static_cast<size_t>(phys) * p.num_kv_heads + h) << p.block_shift) +
-                                    (key & (p.block_size - 1))) * kHeadDim;
-                const uint4* src = reinterpret_cast<const uint4*>(cache + off);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x8[e] = __ldg(src + e);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x8[e] = make_uint4(0, 0, 0, 0);
-            }
-        };
-        auto widen_store = [&](uint8_t* stage, int u, const uint4 (&x8)[8]) {
-            // 128 e4m3 codes -> exact f16, two d-halves, 128-byte swizzle
-            const int row = 64 * u + krow;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t w[4] = {x8[e].x, x8[e].y, x8[e].z, x8[e].w};
-                uint32_t f[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    f[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
-                    f[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
-                }
-                uint8_t* dst = stage + (e >> 2) * kKvHalf;
-                *reinterpret_cast<uint4*>(dst + sw128_offset(row, 16 * (e & 3))) = make_uint4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<uint4*>(dst + sw128_offset(row, 16 * (e & 3) + 8)) = make_uint4(f[4], f[5], f[6], f[7]);
-            }
-        };
-        const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
-        const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
-        uint4 xa[8], xb[8];
-        load_item(kc, 0, 0, xa);
-        load_item(kc, 0, 1, xb);
-        for (int i = 0; i < nsteps && ok; ++i) {
-            const int sk = i % kKStages, sv = i % kVStages;
-            if (i >= kKStages && !warp_wait(bar(kBarKEmpty + sk), ((i / kKStages) - 1) & 1, p.timeout_ns)) {
-                ok = false;
-                break;
-            }
-            uint8_t* kdst = sm + kOffK + sk * kKvBytes;
-            widen_store(kdst, 0, xa);
-            load_item(vc, i, 0, xa);
-            widen_store(kdst, 1, xb);
-            load_item(vc, i, 1, xb);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarKFull + sk));
-            if (i >= kVStages && !warp_wait(bar(kBarVEmpty + sv), ((i / kVStages) - 1) & 1, p.timeout_ns)) {
-                ok = false;
-                break;
-            }
-            uint8_t* vdst = sm + kOffV + sv * kKvBytes;
-            widen_store(vdst, 0, xa);
-            load_item(kc, i + 1, 0, xa);
-            widen_store(vdst, 1, xb);
-            load_item(kc, i + 1, 1, xb);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarVFull + sv));
-        }
-        if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
     }
 
     // ---- teardown ----
