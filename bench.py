@@ -266,7 +266,8 @@ def run_ours(args, rank, world, local):
     cascade = bool(args.cascade)
     # the cascade gets the workspace that lets it cut the prefix into key segments
     ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, device=dev, shared_prefix=cascade)
-    outs = [torch.empty_like(w.q[l]) for l in range(w.num_layers)]
+    out_all = torch.empty_like(w.q)                      # [layers, rows, H_q, 128]: one buffer
+    outs = [out_all[l] for l in range(w.num_layers)]
     kv_bytes = kv_read_bytes(w)
     if cascade and not (w.is_decode_only and w.shared_prefix_blocks > 0):
         raise SystemExit("--cascade needs a decode workload whose tables share leading blocks (shared-prefix)")
@@ -349,7 +350,7 @@ def run_ours(args, rank, world, local):
         chunk = (sum(a.elapsed_time(b) for a, b in cev) / args.steps, chunk_flops(w))
 
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(args, w, pa, ws, outs, layers_caches, dev) if not args.no_e2e else None
+    e2e = run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all) if not args.no_e2e else None
 
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -436,7 +437,7 @@ def run_ours(args, rank, world, local):
     return line
 
 
-def run_e2e(args, w, pa, ws, outs, layers_caches, dev):
+def run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all):
     """Same metric through the public API, with the step's inputs copied from pinned
     host memory and the outputs copied back inside the timed region.  The copies run
     on two copy streams beside the attention: the first layer's inputs go first, the
@@ -448,7 +449,8 @@ def run_e2e(args, w, pa, ws, outs, layers_caches, dev):
     shared = [w.slot_mapping, w.block_tables, w.seq_lens, w.query_start_loc]
     pinned_layer = [t.detach().cpu().pin_memory() for t in per_layer]
     pinned_shared = [t.detach().cpu().pin_memory() for t in shared]
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    host_all = torch.empty((len(outs),) + tuple(outs[0].shape), dtype=outs[0].dtype, pin_memory=True)
+    host_out = [host_all[l] for l in range(len(outs))]
     h2d = sum(t.numel() * t.element_size() for t in pinned_layer + pinned_shared)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     copy_in, copy_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -475,11 +477,18 @@ def run_e2e(args, w, pa, ws, outs, layers_caches, dev):
                 comp.wait_event(first if layer == 0 else rest)
 
         def after(layer):
+            # the outputs of all layers but the last go back in one copy while the last
+            # layer runs, then the last layer's (outs are the layers of out_all)
+            if layer < layers - 2:
+                return
             done = torch.cuda.Event()
             done.record(comp)
             copy_out.wait_event(done)
             with torch.cuda.stream(copy_out):
-                host_out[layer].copy_(outs[layer], non_blocking=True)
+                if layer == layers - 2:
+                    host_all[:layers - 1].copy_(out_all[:layers - 1], non_blocking=True)
+                else:
+                    host_all[layers - 1].copy_(out_all[layers - 1], non_blocking=True)
 
         build_step(w, pa, ws, outs, layers_caches, cascade=bool(args.cascade), before_layer=before,
                    after_layer=after)
