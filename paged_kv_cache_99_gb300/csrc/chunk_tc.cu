@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 auto issue_s = [&](int x, int i) {
                     const uint32_t qbase = sbase + kOffQ + x * 2 * kQHalf;
                     const uint32_t kbase = sbase + kOffK + (i % kKStages) * kKvBytes;
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                         const uint64_t a = umma_desc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
                         const uint64_t b = umma_desc_sw128(kbase + (kk >> 2) * kKvHalf + (kk & 3) * 32, 16, 1024);
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 };
                 auto issue_pv = [&](int x, int j) {
                     const uint32_t vbase = sbase + kOffV + (j % kVStages) * kKvBytes;
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                         // V is MN-major: d-halves kKvHalf apart, 16 keys = 2 KiB
                         const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 uint32_t idle = 0;
                 while (ok && (next_pv[0] < tile_steps(0) || next_pv[1] < tile_steps(1))) {
                     bool progress = false;
-    #pragma unroll
+#pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         const int other = 1 - x;
                         const int j = next_pv[x];
@@ -434,21 +434,21 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     const size_t off = (((static_cast<size_t>(phys) * p.num_kv_heads + h) << p.block_shift) +
                                         (key & (p.block_size - 1))) * kHeadDim;
                     const uint4* src = reinterpret_cast<const uint4*>(cache + off);
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 8; ++e) x8[e] = __ldg(src + e);
                 } else {
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 8; ++e) x8[e] = make_uint4(0, 0, 0, 0);
                 }
             };
             auto widen_store = [&](uint8_t* stage, int u, const uint4 (&x8)[8]) {
                 // 128 e4m3 codes -> exact f16, two d-halves, 128-byte swizzle
                 const int row = 64 * u + krow;
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const uint32_t w[4] = {x8[e].x, x8[e].y, x8[e].z, x8[e].w};
                     uint32_t f[8];
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         f[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
                         f[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
