@@ -9,24 +9,24 @@
 //
 // One CTA = two consecutive tiles A and B of 128 MMA rows each (queries x all
 // heads of one KV head, so every K/V tile in shared memory serves the whole
-// GQA group twice) of one chunk; keys advance 128 at a time (8 blocks).  A
-// kind::f16 MMA costs the tensor core about the same time for any N up to 128,
-// so both products run at N = 128: S = Q K^T over 128 keys and O += P V over
+// GQA group twice) of one chunk; keys advance 128 at a time (8 blocks).  Both
+// products run at N = 128 (a kind::f16 MMA with M = 128, N = 128, K = 16 takes
+// the tensor core 64 cycles): S = Q K^T over 128 keys and O += P V over
 // d = 128.  While one softmax warpgroup works on its tile, the tensor core runs
-// the other tile's products (ping-pong).
+// the other tile's products (ping-pong).  Twelve warps, three warpgroups:
 //   warp 0       producer: bulk tensor copies (TMA, 128-byte swizzle) of each
 //                step's K blocks and V blocks (16-bit caches) into separate
-//                2-stage rings, one lane per block
+//                2-stage rings, one lane per block, K of step i+1 before V of i
 //   warp 1       one lane issues tcgen05.mma: S_X(i) = Q_X K_i^T into tensor
 //                memory, O_X += P_X(i) V_i with P_X read from tensor memory
-//   warps 2-5    softmax of tile A, warps 6-9 softmax of tile B: one thread
+//   warps 2, 3   FP8 caches only: gather e4m3 rows through the block table,
+//                widen them exactly to f16 and store them in the MMA layout
+//   warps 4-7    softmax of tile A, warps 8-11 softmax of tile B: one thread
 //                per row holds its 128 scores in registers (one tensor-memory
 //                read per step), causal mask, online max/sum, P (16-bit)
 //                written back over the columns of S; O rescaled in tensor
 //                memory only when a row maximum grows by more than 2^8
-//   warps 0, 10  FP8 caches only (in place of the producer): gather e4m3 rows
-//                through the block table, widen them exactly to f16 and store
-//                them in the MMA layout
+// Warps 0-3 give registers to the softmax warpgroups (setmaxnreg).
 // Per tile the chain is S(i) -> softmax(i) -> P.V(i) -> S(i+1): S(i+1) reuses
 // the columns P(i) sits in, and the tensor core runs one thread's MMAs in
 // order, so the completion of S(i+1) also means P.V(i) is done.
