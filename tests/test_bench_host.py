@@ -61,3 +61,37 @@ def test_reference_arm_prints_contract_line(capsys):
     assert line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+class _RecordingPa:
+    """Stands in for the library: records which entry point each layer calls."""
+
+    def __init__(self, log):
+        self.log = log
+
+    def __getattr__(self, name):
+        def call(*args, **kwargs):
+            self.log.append(name)
+        return call
+
+
+def test_step_hooks_wrap_each_layer_in_order():
+    # the end-to-end step hangs its copies on these hooks: each layer's input wait
+    # before its calls, its output copy after them
+    w = W.qwen25_15b("cpu", num_layers=3, batch=2)
+    log = []
+    caches = [(w.k_cache[l], w.v_cache[l]) for l in range(w.num_layers)]
+    outs = [torch.empty_like(w.q[l]) for l in range(w.num_layers)]
+    bench.build_step(w, _RecordingPa(log), None, outs, caches,
+                     before_layer=lambda l: log.append(f"before {l}"), after_layer=lambda l: log.append(f"after {l}"))
+    want = []
+    for l in range(3):
+        want += [f"before {l}", "pa_decode_append", f"after {l}"]
+    assert log == want
+    # a mixed batch: slot write, then the mixed call, per layer
+    wm = W.build_workload(name="m", seed=1, device="cpu", num_layers=2, seq_lens=[40, 90], q_lens=[1, 30],
+                          num_q_heads=16, num_kv_heads=2)
+    log.clear()
+    bench.build_step(wm, _RecordingPa(log), None, [torch.empty_like(wm.q[l]) for l in range(2)],
+                     [(wm.k_cache[l], wm.v_cache[l]) for l in range(2)])
+    assert log == ["pa_reshape_and_cache", "pa_mixed"] * 2
