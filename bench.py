@@ -138,26 +138,29 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {"decode": "decode.cu", "chunk": "chunk_tc.cu"}
+
+
+def kernel_source_hash(kernel: str = "decode") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_99_gb300", "csrc")
-    for name in ("decode.cu", "pa_device.cuh", "pa_internal.h"):
+    for name in (KERNEL_SOURCES[kernel], "pa_device.cuh", "pa_internal.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per decode launch from a committed ncu summary, if it was taken
-    on the current decode kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+def recorded_traffic(workload: str, kernel: str = "decode"):
+    """DRAM bytes per launch of the workload's decode (or chunk) kernel from a
+    committed ncu summary, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
     ent = rec.get(workload)
-    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -427,7 +430,7 @@ def run_ours(args, rank, world, local):
             "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)" if peak_src == "measured" else "fallback",
             "unit": "TFLOP/s",
             "frac": round(c_achieved / tpeak, 4),
-            "traffic": None,
+            "traffic": recorded_traffic(args.workload, "chunk"),
             "algorithmic_flops_per_launch": c_flops,
             "avg_launch_ms": round(c_ms, 5),
         }
