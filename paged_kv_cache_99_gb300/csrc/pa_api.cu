@@ -179,9 +179,9 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     const bool append = slots != nullptr;
     // claimed pieces balance SMs that stream at different rates; they pay only where
     // workers' ranges are long (judged from the table width: the decode grid decides
-    // from the lengths) and the warps keep HBM busy: FP8 warps are bound by the
-    // latency of each block, not by HBM, and lose more to the pieces than the
-    // balance gains.  A mixed batch's decode grid starts beside the chunk grid, CTA
+    // from the lengths) and the warps keep HBM busy: FP8 warps, and 16-bit warps with
+    // more than 4 query heads per unit, are bound by the latency of each block, not
+    // by HBM, and lose more to the pieces than the balance gains.  A mixed batch's decode grid starts beside the chunk grid, CTA
     // by CTA, and a cascade's beside the prefix grid, whose end it rarely sets: both
     // keep static ranges
     const int hg0 = head_groups_of(num_q_heads, num_kv_heads);
@@ -190,7 +190,9 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     const long long t_max = units_max * per_unit_max;
     const int w_default = st->sms * kMaxDecodeCtasPerSm * kDecodeWarps;
     const int w_est = num_workers > 0 ? num_workers : w_default;
-    const bool dyn = query_start_loc == nullptr && !cascade && kind != kKindFp8 && t_max / w_est >= kMinPieceRange;
+    const int unit_heads = num_q_heads / num_kv_heads < kHeadsPerGroup ? num_q_heads / num_kv_heads : kHeadsPerGroup;
+    const bool dyn = query_start_loc == nullptr && !cascade && kind != kKindFp8 && unit_heads <= 4 &&
+                     t_max / w_est >= kMinPieceRange;
     const size_t smem = decode_smem_bytes(kind, num_seqs);
     if (smem + 1024 > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
     int ctas = 0;
