@@ -297,7 +297,8 @@ def test_claimed_pieces_many_calls_one_workspace(workers):
 
 def test_claimed_pieces_after_a_timeout_and_other_calls():
     # a timed-out call, a plain decode and a mixed batch in between leave the counter usable
-    w = _case(64, [2000, 3000, 100], 8, write_new=False)
+    # (units of 4 query heads: the ones that take claimed pieces)
+    w = _case(64, [2000, 3000, 100], 4, write_new=False)
     ws = pa.new_workspace(16, 64, 8)
     pa.pa_selftest_wait_timeout(ws, 2000)
     assert pa.pa_read_device_status(ws) == pa.PA_ERR_TIMEOUT
