@@ -40,7 +40,7 @@ METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and seq-steps/sec
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-DEFAULT_WORKLOAD = "qwen2.5-1.5b"
+DEFAULT_WORKLOAD = "gqa40-8k"
 DESCRIPTIONS = {
     "tiny": "tiny decode: 1 layer, B=4, seq_lens 8/17/31/46, H_q=8, H_kv=2, d=128, block 16, bf16",
     "qwen2.5-1.5b": "Qwen2.5-1.5B-shaped decode: 28 layers, B=64, H_q=12, H_kv=2, d=128, block 16, bf16, "
@@ -54,6 +54,8 @@ DESCRIPTIONS = {
                         "prefix blocks and no private tokens (the decode's L2 ceiling for shared blocks)",
     "mixed-fp8": "mixed fp8: 1 layer, H_q=64, H_kv=8, e4m3 KV, 16 decode rows (lognormal median 8192, cap 32768) "
                  "+ 2 prefill chunks of 512 on 4096-token contexts",
+    "mixed-bf16": "mixed bf16: 1 layer, H_q=64, H_kv=8, bf16 KV, 16 decode rows (lognormal median 8192, cap 32768) "
+                  "+ 2 prefill chunks of 512 on 4096-token contexts",
 }
 ELEM = {"bf16": 2, "fp16": 2, "fp8": 1}
 
@@ -63,8 +65,12 @@ def kv_read_bytes(w: W.Workload) -> int:
     return w.num_layers * int(w.seq_lens.sum().item()) * 2 * w.num_kv_heads * w.head_dim * ELEM[w.cache_dtype]
 
 
-def describe(name: str, block_size: int) -> str:
+def describe(name: str, block_size: int, num_layers: int | None = None) -> str:
     d = DESCRIPTIONS.get(name, name)
+    full = {"qwen2.5-1.5b": 28, "gqa40-8k": 40}.get(name)
+    if num_layers is not None and full is not None and num_layers != full:
+        d = d.replace(f"{full} layers", f"{num_layers} of {full} layers").replace(
+            "40-layer GQA decode", f"40-layer GQA decode ({num_layers} layer{'s' if num_layers > 1 else ''} run)")
     if block_size != W.BLOCK_SIZE:
         d = d.replace("block 16", f"block {block_size}").replace(
             "128 aliased prefix blocks", f"2048-token aliased prefix ({2048 // block_size} blocks of {block_size})").replace(
@@ -245,7 +251,10 @@ def enqueue_layer(w: W.Workload, pa, ws, outs, layers_caches, layer, decode_only
                     w.max_q_len, w.scale, ws, ks, vs)
 
 
-def capture(fn):
+def capture(fn, counted=None):
+    """CUDA graph of fn's launches; with `counted` (a list), the number of the
+    library's kernels in the graph is appended to it."""
+    import paged_kv_cache_99_gb300 as pa
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -253,20 +262,49 @@ def capture(fn):
         fn()          # warm the library's per-device caches outside capture
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
+    before = pa.pa_kernel_launches()
     with torch.cuda.graph(g):
         fn()
     torch.cuda.synchronize()
+    if counted is not None:
+        counted.append(pa.pa_kernel_launches() - before)
     return g
 
 
-def run_ours(args, rank, world, local):
+def timed_steps(run_step, steps, min_region_s, est_ms, world):
+    """Device time of K steps, repeated in passes until the timed region spans at
+    least min_region_s (so that the clock record holds enough samples).  Every
+    step is bracketed by its own CUDA events on the launching stream; the region
+    by a barrier and a synchronize on both sides.  Returns (ms per step, max over
+    ranks), passes, wall seconds of the region."""
+    passes = max(1, math.ceil(min_region_s * 1e3 / max(est_ms * steps, 1e-3)))
+    passes = int(reduce_max(float(passes), world))
+    n = passes * steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n):
+        run_step(ev[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    ms_local = sum(a.elapsed_time(b) for a, b in ev) / n
+    return reduce_max(ms_local, world), passes, wall
+
+
+def measure(args, name, dev, world, rank, cascade=False, num_layers=None, e2e=True, cpu=False, steps=None):
+    """One workload: the step graph timed over the region, the dominant kernel's
+    roofline, optionally the end-to-end number and the CPU oracle baseline."""
     import paged_kv_cache_99_gb300 as pa
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    # every replica runs the same workload (weak scaling)
-    w = W.make(args.workload, dev, **({"block_size": args.block_size} if args.block_size != W.BLOCK_SIZE else {}))
+    steps = steps or args.steps
+    kw = {}
+    if args.block_size != W.BLOCK_SIZE:
+        kw["block_size"] = args.block_size
+    if num_layers is not None:
+        kw["num_layers"] = num_layers
+    w = W.make(name, dev, **kw)
     layers_caches = [(w.k_cache[l], w.v_cache[l]) for l in range(w.num_layers)]
-    cascade = bool(args.cascade)
     # the cascade gets the workspace that lets it cut the prefix into key segments
     ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, device=dev, shared_prefix=cascade)
     out_all = torch.empty_like(w.q)                      # [layers, rows, H_q, 128]: one buffer
@@ -274,61 +312,49 @@ def run_ours(args, rank, world, local):
     kv_bytes = kv_read_bytes(w)
     if cascade and not (w.is_decode_only and w.shared_prefix_blocks > 0):
         raise SystemExit("--cascade needs a decode workload whose tables share leading blocks (shared-prefix)")
-    step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, cascade=cascade))
+    # the library's kernels per step, counted as the step graph is captured
+    counted = []
+    step_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, cascade=cascade), counted)
     decode_graph = capture(lambda: build_step(w, pa, ws, outs, layers_caches, decode_only_kernels=True,
                                               cascade=cascade))
-    # per layer: the slot write (fused into the decode kernel in a decode step), the
-    # attention kernel and its combine, the chunk kernel of a mixed batch or cascade
     fused = w.is_decode_only and w.num_new_tokens and not cascade
-    launches_per_step = w.num_layers * ((1 if w.num_new_tokens and not fused else 0) + 2 +
-                                        (0 if w.is_decode_only and not cascade else 1))
+    launches_per_step = counted[0]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     unique_bytes = sum(c.numel() * c.element_size() * 2 for c in w.k_cache)
     flush = unique_bytes < 2 * l2
     flush_buf = torch.empty(4 * l2, dtype=torch.uint8, device=dev) if flush else None
 
-    def one_step():
+    def step_with(ev, graph):
         if flush:
             flush_buf.fill_(1)
-        step_graph.replay()
+        ev[0].record()
+        graph.replay()
+        ev[1].record()
 
-    for _ in range(args.warmup):
-        one_step()
+    warm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.warmup)]
+    step_with(warm[0], step_graph)
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for e in warm[1:]:
+        step_with(e, step_graph)
+    torch.cuda.synchronize()
+    # wall time per step, L2 flush included: sizes the passes of the timed region
+    est_ms = (time.perf_counter() - t0) * 1e3 / max(1, len(warm) - 1)
     status = pa.pa_read_device_status(ws)
     if status != pa.PA_OK:
         raise RuntimeError(f"device status after warm-up: {pa.pa_status_string(status)}")
 
-    # ---- timed region: K steps, per-step device time by events ----
-    clocks = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        if flush:
-            flush_buf.fill_(1)
-        ev[i][0].record()
-        step_graph.replay()
-        ev[i][1].record()
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    barrier(world)
+    # ---- timed region: K steps per pass, passes until the region spans min_region_s ----
+    clocks = ClockSampler(int(dev.index or 0))
+    ms, passes, t_wall = timed_steps(lambda e: step_with(e, step_graph), steps, args.min_region_s, est_ms, world)
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms_local = sum(step_ms) / len(step_ms)
-    ms = reduce_max(ms_local, world)
 
-    # ---- decode kernel alone, same inputs: average launch duration ----
-    dg_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        if flush:
-            flush_buf.fill_(1)
-        dg_ev[i][0].record()
-        decode_graph.replay()
-        dg_ev[i][1].record()
+    # ---- the attention calls alone (no separate slot write), same inputs: average call duration ----
+    dg_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e in dg_ev:
+        step_with(e, decode_graph)
     torch.cuda.synchronize()
-    dec_ms = sum(a.elapsed_time(b) for a, b in dg_ev) / args.steps / w.num_layers
+    dec_ms = sum(a.elapsed_time(b) for a, b in dg_ev) / steps / w.num_layers
 
     # ---- a mixed batch is dominated by the chunk kernel: time it on the chunk rows alone ----
     chunk = None
@@ -342,18 +368,14 @@ def run_ours(args, rank, world, local):
         cg = capture(lambda: pa.pa_mixed(cout, cq, cqsl, kc, vc, cbt, csl, cmax, w.scale, cws, ks, vs))
         for _ in range(3):
             cg.replay()
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for i in range(args.steps):
-            if flush:
-                flush_buf.fill_(1)
-            cev[i][0].record()
-            cg.replay()
-            cev[i][1].record()
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e in cev:
+            step_with(e, cg)
         torch.cuda.synchronize()
-        chunk = (sum(a.elapsed_time(b) for a, b in cev) / args.steps, chunk_flops(w))
+        chunk = (sum(a.elapsed_time(b) for a, b in cev) / steps, chunk_flops(w))
 
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all) if not args.no_e2e else None
+    e2e_line = run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all, cascade, steps) if e2e else None
 
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -365,13 +387,14 @@ def run_ours(args, rank, world, local):
         tok += w.shared_prefix_blocks * w.block_size
         per_launch_bytes = tok * 2 * w.num_kv_heads * w.head_dim * ELEM[w.cache_dtype]
     achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = None if cascade else recorded_traffic(args.workload)
+    # one layer's launch reads the same bytes whatever the number of layers
+    traffic = None if cascade else recorded_traffic(name)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 5),
         "higher_is_better": True,
@@ -380,8 +403,9 @@ def run_ours(args, rank, world, local):
         "dtype": w.cache_dtype,
         "data": "synthetic",
         "config": {
-            "workload": describe(args.workload, w.block_size),
-            "name": args.workload,
+            "workload": describe(name, w.block_size, w.num_layers),
+            "name": name,
+            "num_layers": w.num_layers,
             "block_size": w.block_size,
             "last_block_waste": last_block_waste(w),
             "kv_bytes_per_step": kv_bytes,
@@ -390,28 +414,34 @@ def run_ours(args, rank, world, local):
                          ("pa_reshape_and_cache + " if w.num_new_tokens else "")
                          + (("pa_decode_shared_prefix" if cascade else "pa_decode") if w.is_decode_only
                             else "pa_mixed")) + ")",
-            "l2": ("L2 flushed between steps" if flush else
+            "l2": ("L2 flushed between steps (a 4 x L2 buffer written before each)" if flush else
                    f"inputs larger than L2 ({unique_bytes / 1e9:.2f} GB of cache vs {l2 / 1e6:.0f} MB L2)"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
+        "timed_region": {"passes": passes, "steps_timed": passes * steps, "wall_s": round(t_wall, 3),
+                         "ms_per_step": "mean over every timed step"},
         "seq_steps_per_s": round(w.num_seqs * world / (ms * 1e-3), 1),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / hbm_peak, 2),
         "roofline": {
             "kernel": "pa_decode_shared_prefix (unique bytes: prefix once + suffixes)" if cascade else
-                      ("pa_decode_append" if fused else "pa_decode"),
+                      ("pa_decode_append" if fused else
+                       ("pa_decode (logical bytes: shared blocks counted per table)" if w.shared_prefix_blocks
+                        else "pa_decode")),
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": hbm_peak,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
             "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4),
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
             "traffic": traffic,
             "algorithmic_bytes_per_launch": per_launch_bytes,
             "avg_launch_ms": round(dec_ms, 5),
         },
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e_line,
+        "gpu_launches": launches_per_step * passes * steps,
+        "launches_per_step": launches_per_step,
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
     }
@@ -430,17 +460,49 @@ def run_ours(args, rank, world, local):
             "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)" if peak_src == "measured" else "fallback",
             "unit": "TFLOP/s",
             "frac": round(c_achieved / tpeak, 4),
-            "traffic": recorded_traffic(args.workload, "chunk"),
+            "traffic": recorded_traffic(name, "chunk"),
             "algorithmic_flops_per_launch": c_flops,
             "avg_launch_ms": round(c_ms, 5),
         }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and cpu:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         line["cpu_baseline"]["kv_bytes_per_step"] = kv_bytes
+    del step_graph, decode_graph, w, layers_caches, ws, out_all, outs, flush_buf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     return line
 
 
-def run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all):
+# the benchmark spec's targets besides the headline: measured in the same run, each with
+# its own timed region and clock record
+TARGETS = (("shared-prefix", "shared-prefix", False), ("shared-prefix-cascade", "shared-prefix", True),
+           ("mixed-fp8", "mixed-fp8", False))
+
+
+def target_summary(line):
+    keep = ("value", "unit", "ms_per_step", "steps", "seq_steps_per_s", "pct_of_nominal_hbm", "pct_of_measured_hbm",
+            "roofline", "roofline_decode_rows", "clocks", "timed_region", "gpu_launches")
+    out = {"workload": line["config"]["workload"], "launch": line["config"]["launch"], "l2": line["config"]["l2"],
+           "kv_bytes_per_step": line["config"]["kv_bytes_per_step"]}
+    out.update({k: line[k] for k in keep if k in line})
+    return out
+
+
+def run_ours(args, rank, world, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    # every replica runs the same workload (weak scaling)
+    line = measure(args, args.workload, dev, world, rank, cascade=bool(args.cascade), num_layers=args.layers,
+                   e2e=not args.no_e2e, cpu=not args.no_cpu_baseline)
+    if not args.no_targets and args.workload == DEFAULT_WORKLOAD and not args.cascade and args.layers is None:
+        line["targets"] = {}
+        for key, name, casc in TARGETS:
+            t = measure(args, name, dev, world, rank, cascade=casc, e2e=False, cpu=False)
+            line["targets"][key] = target_summary(t)
+    return line
+
+
+def run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all, cascade, steps):
     """Same metric through the public API, with the step's inputs copied from pinned
     host memory and the outputs copied back inside the timed region.  The copies run
     on two copy streams beside the attention: the first layer's inputs go first, the
@@ -493,8 +555,7 @@ def run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all):
                 else:
                     host_all[layers - 1].copy_(out_all[layers - 1], non_blocking=True)
 
-        build_step(w, pa, ws, outs, layers_caches, cascade=bool(args.cascade), before_layer=before,
-                   after_layer=after)
+        build_step(w, pa, ws, outs, layers_caches, cascade=cascade, before_layer=before, after_layer=after)
         comp.wait_stream(copy_out)
         comp.wait_stream(copy_in)
 
@@ -509,11 +570,11 @@ def run_e2e(args, w, pa, ws, outs, layers_caches, dev, out_all):
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
+    ms = a.elapsed_time(b) / steps
     return {"value": round(kv_read_bytes(w) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -531,7 +592,10 @@ def raw(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-def cpu_baseline(w: W.Workload, seconds: float, total_layers: int | None = None):
+REF_SAMPLE_SEQS = 8
+
+
+def cpu_baseline(w: W.Workload, seconds: float, total_layers: int | None = None, total_seqs: int | None = None):
     """The oracle as it stands, single-threaded, on a bounded sample of the
     workload: whole layers (slot write + attention for every sequence) until
     `seconds` of oracle time have passed; reported in the same unit (KV GB/s)."""
@@ -558,8 +622,10 @@ def cpu_baseline(w: W.Workload, seconds: float, total_layers: int | None = None)
         elapsed += time.perf_counter() - t1
         layers += 1
     return {"value": round(layers * per_layer / elapsed / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{layers} of {total_layers or w.num_layers} layers, every sequence, slot write + attention, "
-                      f"float64, one thread (host has {os.cpu_count()} cores)",
+            "sample": f"{layers} of {total_layers or w.num_layers} layers, "
+                      + (f"{w.num_seqs} of {total_seqs} sequences" if total_seqs else "every sequence")
+                      + f", slot write + attention, float64, one thread (host has {os.cpu_count()} cores); "
+                      "the rate is per KV byte, so it stands for the whole step",
             "seconds": round(elapsed, 3)}
 
 
@@ -569,13 +635,16 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     kw = {"num_layers": 1} if args.workload in ("qwen2.5-1.5b", "gqa40-8k") else {}
+    if args.workload == "gqa40-8k":
+        kw["batch"] = REF_SAMPLE_SEQS       # a sample of the 40 equal sequences: the rate is per byte
     if args.block_size != W.BLOCK_SIZE:
         kw["block_size"] = args.block_size
     w = W.make(args.workload, "cpu", **kw)
     total = {"qwen2.5-1.5b": 28, "gqa40-8k": 40}.get(args.workload, w.num_layers)
+    seqs = {"gqa40-8k": 40}.get(args.workload)
     per_step = []
     for _ in range(args.warmup + args.steps):
-        per_step.append(cpu_baseline(w, args.ref_step_seconds, total))
+        per_step.append(cpu_baseline(w, args.ref_step_seconds, total, seqs))
     timed = per_step[args.warmup:]
     value = statistics.mean(x["value"] for x in timed)
     ms = statistics.mean(1e3 * x["seconds"] for x in timed)
@@ -656,6 +725,12 @@ def main(argv=None):
                     help="copy-blocks: time the copy-on-write block copies instead of the attention step")
     ap.add_argument("--block-size", type=int, default=W.BLOCK_SIZE, choices=[8, 16, 32],
                     help="tokens per cache block (the named workloads are built with 16)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only this many layers of a multi-layer workload (e.g. 1 for an ncu capture)")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the shared-prefix, cascade and mixed-fp8 measurements that follow the default headline")
+    ap.add_argument("--min-region-s", type=float, default=2.5,
+                    help="repeat the K timed steps in passes until the timed region spans this many seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)

@@ -86,6 +86,12 @@ PA_API const char* pa_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 PA_API int pa_version(void);
 
+/* Kernels this library has enqueued in this process (every entry point counts the
+ * launches it makes; a launch into a stream being captured counts once, at
+ * capture).  A caller can read it before and after a call to see how many kernels
+ * the call launches. */
+PA_API unsigned long long pa_kernel_launches(void);
+
 /* Text of the last CUDA failure seen by a call of this thread that returned
  * PA_ERR_CUDA (which CUDA call failed and its error string); "" if none.  The
  * buffer is thread-local and valid until the next failing call. */
@@ -209,6 +215,21 @@ PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, c
                                   const float* k_scale, const float* v_scale, void* workspace,
                                   size_t workspace_bytes, pa_stream_t stream);
 
+/* pa_decode_append with an explicit worker count (1 .. pa_default_workers(); 0 =
+ * the default), as pa_decode_ex is to pa_decode.  The cache bytes it writes do not
+ * depend on the worker count; outputs agree with pa_decode_append to rounding.
+ * With long ranges per worker (>= 48 16-key units, 16-bit cache, at most 4
+ * query heads per KV head) the last ~10% of the work is handed out at run time
+ * in pieces, so a small worker count is how a small batch reaches that path. */
+PA_API pa_status pa_decode_append_ex(void* out, const void* q, const void* k_new, const void* v_new,
+                                     const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int num_blocks, float scale,
+                                     pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale,
+                                     const float* v_scale, void* workspace, size_t workspace_bytes,
+                                     int num_workers, pa_stream_t stream);
+
 /* pa_decode with an explicit worker count (1 .. pa_default_workers(); 0 = the
  * default).  Fewer workers means longer ranges per worker and fewer split
  * points; results agree with pa_decode to rounding. */
@@ -300,20 +321,28 @@ PA_API pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_l
  * every GPU that loads the library holds it until the process exits.  This call
  * allocates nothing and calls no allocating routine.
  *
- *  - Limit: the batch must fit the 16 MiB scratch: 256 + 4 (num_seqs + 2)
- *    (rounded up to 256) + 4160 (W + num_seqs * num_kv_heads * ceil(G / 8))
- *    bytes, W = pa_default_workers() (1216 on a 152-SM GB300, which allows
- *    about 2800 sequence x KV-head units, e.g. 350 sequences with 8 KV heads).
- *    Larger batches return PA_ERR_WORKSPACE with the sizes in pa_last_error().
+ *  - Limit: the batch must fit the 16 MiB scratch.  With S = num_seqs,
+ *    G = num_q_heads / num_kv_heads, W = pa_default_workers() (1216 on a 152-SM
+ *    GB300), N = S * num_kv_heads * ceil(G / 8) + 2 W partial slots and R(x) = x
+ *    rounded up to a multiple of 256, a call needs
+ *        256 + R(4 (S + 1)) + R(512 S num_q_heads) + R(8 S num_q_heads)
+ *            + R(64 N) + 4096 N
+ *    bytes; the 2 W slots alone take about 10.1 MB on a 152-SM GB300.  There
+ *    that allows at most 100 sequences with 64 query and 8 KV heads, 133 with
+ *    32 and 8, 177 with 8 and 8, 457 with 12 and 2, 533 with 8 and 2.  Larger
+ *    batches return PA_ERR_WORKSPACE with the sizes in pa_last_error().
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current and caches it; make that
  *    first call before any stream capture.
  *  - All calls share the one array, which keeps the previous call's contents;
- *    each call clears the part that must start at zero (the status word) on its
- *    stream.  Calls that may overlap on the GPU (other streams, other threads)
+ *    each call clears the part that must start at zero (the status word and
+ *    the work counter at its head) on its stream.  Calls that may overlap on the GPU (other streams, other threads)
  *    race on the array and give undefined results: serialise them.
- *  - Device-side reports (PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT) stay in the
- *    static array and are not returned by this call.
+ *  - Device-side reports (PA_ERR_OUT_OF_RANGE for a bad block-table entry,
+ *    PA_ERR_TIMEOUT) stay in the static array, where no caller can read them,
+ *    and the next call clears them: this call cannot report them.  A caller
+ *    that needs those checks must use pa_decode with a workspace and read it
+ *    with pa_read_device_status.
  */
 PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int max_blocks_per_seq,

@@ -53,6 +53,8 @@ def _lib():
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
     lib.pa_version.restype = I
+    lib.pa_kernel_launches.argtypes = []
+    lib.pa_kernel_launches.restype = ctypes.c_ulonglong
     lib.pa_last_error.argtypes = []
     lib.pa_last_error.restype = ctypes.c_char_p
     lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
@@ -68,6 +70,8 @@ def _lib():
     lib.pa_decode_ex.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, I, P]
     lib.pa_decode_append.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
     lib.pa_decode_append.restype = I
+    lib.pa_decode_append_ex.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P, P, Z, I, P]
+    lib.pa_decode_append_ex.restype = I
     lib.pa_decode_ex.restype = I
     lib.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, F, I, I, P, P, P, Z, P]
     lib.pa_decode_shared_prefix.restype = I
@@ -145,6 +149,12 @@ def pa_status_string(status: int) -> str:
     return _lib().pa_status_string(status).decode()
 
 
+def pa_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process (launches into a captured
+    stream count at capture)."""
+    return int(_lib().pa_kernel_launches())
+
+
 def pa_default_workers() -> int:
     return _lib().pa_default_workers()
 
@@ -207,9 +217,10 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, workspace
 
 
 def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, seq_lens, scale, workspace,
-                     k_scale=None, v_scale=None, stream=None):
+                     k_scale=None, v_scale=None, num_workers: int = 0, stream=None):
     """pa_reshape_and_cache of one new token per sequence (k_new, v_new [B, H_kv, 128] at
-    slot_mapping[B], int64, the slot of position seq_lens[s] - 1) fused with pa_decode."""
+    slot_mapping[B], int64, the slot of position seq_lens[s] - 1) fused with pa_decode;
+    num_workers > 0 goes through pa_decode_append_ex with that worker count."""
     _need(q, "q", (torch.bfloat16, torch.float16))
     _need(out, "out", (q.dtype,))
     for t, n in ((k_new, "k_new"), (v_new, "v_new")):
@@ -225,11 +236,14 @@ def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block
     if (out.shape != q.shape or block_tables.shape[0] != B or seq_lens.shape != (B,) or
             k_new.shape != (B, Hkv, d) or v_new.shape != k_new.shape or slot_mapping.shape != (B,)):
         raise ValueError("shape mismatch")
-    st = _lib().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
-                                 _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv,
-                                 d, bs, nb, float(scale), _DTYPE[q.dtype],
-                                 _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale), _ptr(v_scale),
-                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, d, bs, nb, float(scale),
+            _DTYPE[q.dtype], _cache_code(k_cache, k_scale, k_cache.shape[1]), _ptr(k_scale), _ptr(v_scale),
+            _ptr(workspace), workspace.numel())
+    if num_workers:
+        st = _lib().pa_decode_append_ex(*args, int(num_workers), _stream(stream))
+    else:
+        st = _lib().pa_decode_append(*args, _stream(stream))
     _check(st, "pa_decode_append")
 
 

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -33,6 +34,7 @@ std::map<std::tuple<int, int, int, int, int, size_t>, int> g_occupancy;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 thread_local char g_last_error[256] = "";
+std::atomic<unsigned long long> g_launches{0};
 
 pa_status fail(const char* what, cudaError_t e) {
     snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
@@ -45,6 +47,12 @@ pa_status fail_msg(const char* what) {
 }
 
 pa_status cuda_status(cudaError_t e, const char* what) { return e == cudaSuccess ? PA_OK : fail(what, e); }
+
+// Status of a kernel launch; a launch that was enqueued is counted.
+pa_status launched(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(e, what);
+}
 
 // Device attributes of the current device; nullptr on failure.
 DeviceState* device_state(int* dev_out) {
@@ -273,9 +281,9 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = (W + kDecodeWarps - 1) / kDecodeWarps;
-    s = cuda_status(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream), "launch(decode)");
+    s = launched(launch_decode(kind, q_bf16, kmap, vmap, p, grid, smem, stream), "launch(decode)");
     if (s != PA_OK) return s;
-    return cuda_status(launch_combine(q_bf16, kind == kKindFp8, p, 2 * st->sms, stream), "launch(combine)");
+    return launched(launch_combine(q_bf16, kind == kKindFp8, p, 2 * st->sms, stream), "launch(combine)");
 }
 
 pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
@@ -340,7 +348,7 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     p.prefix_ml_extra = prefix_ml_extra;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kDefaultTimeoutNs;
-    return cuda_status(launch_chunk(kind, q_bf16, kmap, vmap, p, static_cast<int>(grid_x), smem, stream),
+    return launched(launch_chunk(kind, q_bf16, kmap, vmap, p, static_cast<int>(grid_x), smem, stream),
                        "launch(chunk)");
 }
 
@@ -433,7 +441,9 @@ const char* pa_status_string(int status) {
     }
 }
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 101; }
+
+unsigned long long pa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* pa_last_error(void) { return g_last_error; }
 
@@ -452,7 +462,7 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
         !aligned(slot_mapping, 8))
         return PA_ERR_INVALID_ARG;
     if (static_cast<long long>(num_tokens) * num_kv_heads >= (1ll << 34)) return PA_ERR_UNSUPPORTED;
-    return cuda_status(launch_reshape(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, num_blocks,
+    return launched(launch_reshape(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, num_blocks,
                                       block_shift_of(block_size), src_dtype == PA_BF16, is_fp8(cache_dtype), k_scale, v_scale, scale_stride_of(cache_dtype),
                                       reinterpret_cast<cudaStream_t>(stream)),
                        "launch(reshape_and_cache)");
@@ -575,12 +585,12 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
                        prefix_units, splits, o_extra, ml_extra);
 }
 
-pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
-                           const int64_t* slot_mapping, void* k_cache, void* v_cache, const int32_t* block_tables,
-                           int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_q_heads,
-                           int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-                           pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
-                           void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+pa_status pa_decode_append_ex(void* out, const void* q, const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping, void* k_cache, void* v_cache, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                              pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                              void* workspace, size_t workspace_bytes, int num_workers, pa_stream_t stream) {
     pa_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                                        scale, q_dtype, cache_dtype, k_scale, v_scale, workspace);
@@ -590,8 +600,21 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
     if (num_seqs == 0) return PA_OK;
     return decode_impl(out, q, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                        num_q_heads, num_kv_heads, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
-                       workspace_bytes, 0, num_blocks, block_size, num_seqs, reinterpret_cast<cudaStream_t>(stream),
-                       false, false, 0, 1, nullptr, nullptr, k_new, v_new, slot_mapping);
+                       workspace_bytes, num_workers, num_blocks, block_size, num_seqs,
+                       reinterpret_cast<cudaStream_t>(stream), false, false, 0, 1, nullptr, nullptr, k_new, v_new,
+                       slot_mapping);
+}
+
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, void* k_cache, void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                           pa_dtype q_dtype, pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                           void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return pa_decode_append_ex(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                               max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, num_blocks, scale, q_dtype, cache_dtype, k_scale, v_scale, workspace,
+                               workspace_bytes, 0, stream);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -682,7 +705,7 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const
     if (workspace && !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
     const size_t block_bytes = static_cast<size_t>(num_kv_heads) * block_size * kHeadDim *
                                (is_fp8(cache_dtype) ? 1 : 2);
-    return cuda_status(launch_copy_blocks(k_cache, v_cache, src, dst, num_pairs, num_blocks, block_bytes,
+    return launched(launch_copy_blocks(k_cache, v_cache, src, dst, num_pairs, num_blocks, block_bytes,
                                           static_cast<int*>(workspace), reinterpret_cast<cudaStream_t>(stream)),
                        "launch(copy_blocks)");
 }
@@ -708,7 +731,7 @@ pa_status pa_selftest_wait_timeout(void* workspace, size_t workspace_bytes, unsi
                                    pa_stream_t stream) {
     if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
     if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return PA_ERR_INVALID_ARG;
-    return cuda_status(launch_wait_selftest(static_cast<int*>(workspace), 1000ull * timeout_us,
+    return launched(launch_wait_selftest(static_cast<int*>(workspace), 1000ull * timeout_us,
                                             reinterpret_cast<cudaStream_t>(stream)),
                        "launch(reshape_and_cache)");
 }

@@ -28,6 +28,7 @@ Named workloads (sizes as the pages' examples and the benchmark suite use them):
                     lengths (median 8192, sigma 1, capped at 32768) plus 2 prefill
                     chunks of 512 queries on 4096-token contexts; the slot write
                     stores all 1040 new tokens.
+``mixed-bf16``      the same batch with a bf16 cache.
 """
 from __future__ import annotations
 
@@ -312,15 +313,21 @@ def shared_prefix_l2(device, seed: int = 1007, batch: int = 128, block_size: int
 
 def mixed_fp8(device, seed: int = 1005, num_decode: int = 16, num_chunks: int = 2,
               chunk_len: int = 512, chunk_ctx: int = 4096, median: int = 8192,
-              sigma: float = 1.0, cap: int = 32768, block_size: int = BLOCK_SIZE) -> Workload:
+              sigma: float = 1.0, cap: int = 32768, block_size: int = BLOCK_SIZE,
+              cache_dtype: str = "fp8", name: str = "mixed-fp8") -> Workload:
     g = torch.Generator(device="cpu").manual_seed(seed)
     z = torch.randn(num_decode, generator=g, dtype=torch.float64)
     dec = [int(min(cap, max(1, round(math.exp(math.log(median) + sigma * float(x)))))) for x in z]
     lens = dec + [chunk_ctx + chunk_len] * num_chunks
     qls = [1] * num_decode + [chunk_len] * num_chunks
-    return build_workload(name="mixed-fp8", seed=seed, device=device, num_layers=1, seq_lens=lens,
+    return build_workload(name=name, seed=seed, device=device, num_layers=1, seq_lens=lens,
                           q_lens=qls, num_q_heads=64, num_kv_heads=8, q_dtype="bf16",
-                          cache_dtype="fp8", block_size=block_size)
+                          cache_dtype=cache_dtype, block_size=block_size)
+
+
+def mixed_bf16(device, seed: int = 1005, block_size: int = BLOCK_SIZE) -> Workload:
+    # the mixed batch with a bf16 cache: the chunk kernel on 16-bit keys and values
+    return mixed_fp8(device, seed=seed, block_size=block_size, cache_dtype="bf16", name="mixed-bf16")
 
 
 NAMED = {
@@ -331,6 +338,7 @@ NAMED = {
     "shared-prefix-long": shared_prefix_long,
     "shared-prefix-l2": shared_prefix_l2,
     "mixed-fp8": mixed_fp8,
+    "mixed-bf16": mixed_bf16,
 }
 
 
