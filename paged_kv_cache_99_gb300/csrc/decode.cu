@@ -318,6 +318,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     int pf_row = -1, pf_want = 0, pf_dst = 0;       // row fetched ahead (-1: none pending)
     long long pf_slot = -1;
     uint4 pf_x = make_uint4(0, 0, 0, 0);
+    // A cascade's private blocks are read once, beside partials (the prefix grid's and
+    // this grid's) that the combine reads back: the stream leaves L2 first, the
+    // partials stay in it
+    const bool stream_first = p.cascade != 0;
+    const uint64_t pol = stream_first ? l2_policy_evict_first() : 0ull;
+    auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+        if (stream_first) tma_load_2d_hint(dst, map, x, y, bar, pol);
+        else tma_load_2d(dst, map, x, y, bar);
+    };
     auto issue = [&](const Cursor& c, int k) {
         // unit ja (16 keys) of the sequence: with blocks of 16 or 32 tokens it lies in
         // table entry 16 ja / bs at row offset 16 ja mod bs; with 8-token blocks it
@@ -367,13 +376,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
             if (bs >= kBlockSize) {
                 mbar_arrive_expect_tx(bar, STAGE);
                 if constexpr (kFp8) {
-                    tma_load_2d(dst, &kmap, 0, y0, bar);
-                    tma_load_2d(dst + TILE, &vmap, 0, y0, bar);
+                    load(dst, &kmap, 0, y0, bar);
+                    load(dst + TILE, &vmap, 0, y0, bar);
                 } else {
-                    tma_load_2d(dst, &kmap, 0, y0, bar);
-                    tma_load_2d(dst + 2048, &kmap, 64, y0, bar);
-                    tma_load_2d(dst + TILE, &vmap, 0, y0, bar);
-                    tma_load_2d(dst + TILE + 2048, &vmap, 64, y0, bar);
+                    load(dst, &kmap, 0, y0, bar);
+                    load(dst + 2048, &kmap, 64, y0, bar);
+                    load(dst + TILE, &vmap, 0, y0, bar);
+                    load(dst + TILE + 2048, &vmap, 64, y0, bar);
                 }
             } else {
                 // 8-row boxes: rows 0-7 of the tile from the first block, 8-15 from the second
@@ -384,13 +393,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
                     const int y = e ? y1 : y0;
                     const uint32_t o = 1024u * e;
                     if constexpr (kFp8) {
-                        tma_load_2d(dst + o, &kmap, 0, y, bar);
-                        tma_load_2d(dst + TILE + o, &vmap, 0, y, bar);
+                        load(dst + o, &kmap, 0, y, bar);
+                        load(dst + TILE + o, &vmap, 0, y, bar);
                     } else {
-                        tma_load_2d(dst + o, &kmap, 0, y, bar);
-                        tma_load_2d(dst + 2048 + o, &kmap, 64, y, bar);
-                        tma_load_2d(dst + TILE + o, &vmap, 0, y, bar);
-                        tma_load_2d(dst + TILE + 2048 + o, &vmap, 64, y, bar);
+                        load(dst + o, &kmap, 0, y, bar);
+                        load(dst + 2048 + o, &kmap, 64, y, bar);
+                        load(dst + TILE + o, &vmap, 0, y, bar);
+                        load(dst + TILE + 2048 + o, &vmap, 64, y, bar);
                     }
                 }
             }
