@@ -534,8 +534,9 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
     if (prefix_units > 0) {
         // Key segments of the prefix (each leaves its own partial rows): only when the
         // prefix grid, 4 us or so per 128-key step of a CTA, would outlast the decode
-        // of the private blocks (bounded from the table width at 5 TB/s), and only as
-        // many as keep the prefix grid on under half the SMs and fit the workspace.
+        // of the private blocks (at 5 TB/s, their mean length taken as half the
+        // table's private width: the lengths are on the device), and only as many as
+        // keep the prefix grid on under half the SMs and fit the workspace.
         const int per_cta = (chunk_rows() / (num_q_heads / num_kv_heads)) * chunk_tiles_per_cta();
         pair_ctas = static_cast<long long>((num_seqs + per_cta - 1) / per_cta) * num_kv_heads;
         const int total_steps = (prefix_units * kBlockSize + 127) / 128;
@@ -543,7 +544,7 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
             static_cast<long long>(max_blocks_per_seq) * block_size - static_cast<long long>(prefix_units) * kBlockSize;
         const double suffix_bytes = static_cast<double>(num_seqs) * num_kv_heads * (suffix_tokens > 0 ? suffix_tokens : 0) *
                                     kHeadDim * 2 * (is_fp8(cache_dtype) ? 1 : 2);
-        const double decode_us = suffix_bytes / 5.0e6;
+        const double decode_us = 0.5 * suffix_bytes / 5.0e6;
         long long cap = (st->sms / 2) / pair_ctas;
         if (cap > total_steps) cap = total_steps;
         if (cap > kMaxPrefixSplits) cap = kMaxPrefixSplits;
