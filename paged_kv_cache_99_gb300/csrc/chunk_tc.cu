@@ -16,9 +16,11 @@
 // the other tile's products (ping-pong).  Twelve warps, three warpgroups:
 //   warp 0       producer: bulk tensor copies (TMA, 128-byte swizzle) of each
 //                step's K blocks and V blocks (16-bit caches) into separate
-//                2-stage rings, one lane per block, K of step i+1 before V of i
-//   warp 1       one lane issues tcgen05.mma: S_X(i) = Q_X K_i^T into tensor
-//                memory, O_X += P_X(i) V_i with P_X read from tensor memory
+//                2-stage rings, one lane per block, K of step i+1 before V of i;
+//                it zeroes the V rows past the CTA's last key in the last step
+//   warp 1       one lane issues tcgen05.mma in a fixed order with suspending
+//                waits: per step O_A += P_A(i) V_i, S_A(i+1) = Q_A K_{i+1}^T, then
+//                the same for tile B (P read from tensor memory)
 //   warps 2, 3   FP8 caches only: gather e4m3 rows through the block table,
 //                widen them exactly to f16 and store them in the MMA layout
 //   warps 4-7    softmax of tile A, warps 8-11 softmax of tile B: one thread
@@ -78,7 +80,8 @@ enum {
     kBarPFull = kBarSFull + 2,              // [tile]
     kBarPvDone = kBarPFull + 2,             // [tile]
     kBarQFull = kBarPvDone + 2,
-    kNumBars = kBarQFull + 1
+    kBarVZero = kBarQFull + 1,              // 16-bit caches: V rows past the CTA's last key zeroed
+    kNumBars = kBarVZero + 1
 };
 static_assert(kNumBars * 8 + 4 <= kBarBytes, "barriers");
 
@@ -162,6 +165,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             mbar_init(bar(kBarPvDone + x), 1);
         }
         mbar_init(bar(kBarQFull), 8);
+        mbar_init(bar(kBarVZero), 1);
         fence_barrier_init();
         if constexpr (!kFp8) {
             tmap_prefetch(&kmap);
@@ -337,6 +341,29 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     y_v = y_k;
                     y_k = y_after;
                 }
+                // keys past the CTA's last position get P = 0, but their V rows hold unloaded
+                // (stale) or poisoned bytes and 0 x NaN is NaN: once the last step's V has
+                // landed, its rows past that position are zeroed before any P.V reads them
+                const int last = nsteps - 1;
+                if (ok && last >= 0) {
+                    const int st = last % kVStages;
+                    if (!warp_wait(bar(kBarVFull + st), (last / kVStages) & 1, p.timeout_ns)) {
+                        ok = false;
+                    } else {
+                        const int first = pos_last_cta - (step0 + last) * kTcKeys + 1;   // first row to zero
+                        uint8_t* vst = sm + kOffV + st * kKvBytes;
+                        for (int r = max(first, 0) + lane; r < kTcKeys; r += 32) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                *reinterpret_cast<uint4*>(vst + r * 128 + 16 * c) = make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4*>(vst + kKvHalf + r * 128 + 16 * c) = make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(kBarVZero));
+                    }
+                }
                 if (!ok && lane == 0) atomicOr(p.status, kDevErrTimeout);
             }
         } else if (warp == 1) {
@@ -364,55 +391,41 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                         umma_f16_ts(tO(x), tS(x) + 8 * kk, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 };
-                // Event loop: poll the barriers and issue whatever is ready, P.V first (the
-                // next S of that tile waits for it), then S.  No barrier tested here can run
-                // a phase ahead: each one's next phase needs an MMA not yet issued.
-                const int zt = has_b ? 1 : 0;             // tile that zeroes V rows in the last step
-                int next_s[2] = {0, 0}, next_pv[2] = {0, 0};
-                ok = mbar_wait_bounded(bar(kBarQFull), 0, p.timeout_ns);
-                uint64_t t_last = 0;
-                uint32_t idle = 0;
-                while (ok && (next_pv[0] < tile_steps(0) || next_pv[1] < tile_steps(1))) {
-                    bool progress = false;
-#pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const int other = 1 - x;
-                        const int j = next_pv[x];
-                        if (j < tile_steps(x) && j < next_s[x] && mbar_test(bar(kBarPFull + x), j & 1) &&
-                            mbar_test(bar(kBarVFull + j % kVStages), (j / kVStages) & 1)) {
-                            // a 16-bit cache's last step also waits for the zeroing tile
-                            const int pv_zt = zt ? next_pv[1] : next_pv[0];
-                            const bool blocked = !kFp8 && j == nsteps - 1 && x != zt && j < tile_steps(zt) &&
-                                                 !(pv_zt > j || mbar_test(bar(kBarPFull + zt), j & 1));
-                            if (!blocked) {
-                                tc_fence_after();
-                                issue_pv(x, j);
-                                next_pv[x] = j + 1;
-                                progress = true;
-                                if (j >= tile_steps(other) || next_pv[other] > j)
-                                    umma_commit(bar(kBarVEmpty + j % kVStages));   // both tiles done with V_j
-                                if (j + 1 == tile_steps(x)) umma_commit(bar(kBarPvDone + x));
-                            }
-                        }
-                        // this tile's next S right behind its P.V, ahead of the other tile's work
-                        const int i = next_s[x];
-                        if (i < tile_steps(x) && next_pv[x] >= i &&
-                            mbar_test(bar(kBarKFull + i % kKStages), (i / kKStages) & 1)) {
+                // Fixed order with suspending waits: per step, P.V(i) of A and A's S(i+1)
+                // right behind it (it reuses the columns P(i) sat in), then the same for B.
+                // Tile A runs about half a step ahead of B, so this is the order in which
+                // the inputs become ready; a waiting issuer sleeps instead of polling.
+                const int na = tile_steps(0), nb = tile_steps(1), nmax = na > nb ? na : nb;
+                auto wait = [&](uint32_t b, uint32_t par) -> bool {
+                    if (ok && !mbar_wait_bounded(b, par, p.timeout_ns)) ok = false;
+                    return ok;
+                };
+                if (wait(bar(kBarQFull), 0) && nmax > 0 && wait(bar(kBarKFull), 0)) {
+                    tc_fence_after();
+                    if (na > 0) issue_s(0, 0);
+                    if (nb > 0) issue_s(1, 0);
+                    umma_commit(bar(kBarKEmpty));
+                }
+                for (int i = 0; i < nmax && ok; ++i) {
+                    const int sv = i % kVStages, sk = (i + 1) % kKStages;
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (i >= tile_steps(x)) continue;
+                        if (!wait(bar(kBarPFull + x), i & 1) || !wait(bar(kBarVFull + sv), (i / kVStages) & 1) ||
+                            (!kFp8 && i == nsteps - 1 && !wait(bar(kBarVZero), 0)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(x, i);
+                        if (i + 1 == tile_steps(x)) umma_commit(bar(kBarPvDone + x));
+                        if (i + 1 < tile_steps(x)) {
+                            if (!wait(bar(kBarKFull + sk), ((i + 1) / kKStages) & 1)) break;
                             tc_fence_after();
-                            issue_s(x, i);
-                            next_s[x] = i + 1;
-                            progress = true;
-                            if (i >= tile_steps(other) || next_s[other] > i)
-                                umma_commit(bar(kBarKEmpty + i % kKStages));       // both tiles done with K_i
+                            issue_s(x, i + 1);
                         }
                     }
-                    if (progress) {
-                        idle = 0;
-                    } else if (++idle == 1) {
-                        t_last = global_timer_ns();
-                    } else if ((idle & 255) == 0 && global_timer_ns() - t_last > p.timeout_ns) {
-                        ok = false;
-                    }
+                    if (!ok) break;
+                    // every P.V(i) is issued: V_i is free; every S(i + 1): K_{i+1} is free
+                    umma_commit(bar(kBarVEmpty + sv));
+                    if (i + 1 < nmax) umma_commit(bar(kBarKEmpty + sk));
                 }
                 if (!ok) atomicOr(p.status, kDevErrTimeout);
             }
@@ -621,28 +634,6 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             f2_unpack(sum2[0], s0, s1);
             f2_unpack(sum2[1], s2, s3);
             l = l * alpha + ((s0 + s1) + (s2 + s3));
-            bool zeroed = false;
-            if constexpr (!kFp8) {
-                // keys past the CTA's last position get P = 0, but their V rows hold unloaded
-                // (stale) or poisoned bytes and 0 x NaN is NaN: the last tile zeroes them
-                if (i == nsteps - 1 && x == (has_b ? 1 : 0)) {
-                    const int st = i % kVStages;
-                    if (!warp_wait(bar(kBarVFull + st), (i / kVStages) & 1, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    if (key0 + r > pos_last_cta) {
-                        uint8_t* vrow = sm + kOffV + st * kKvBytes + r * 128;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
-                            *reinterpret_cast<uint4*>(vrow + kKvHalf + 16 * c) = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                    zeroed = true;
-                }
-            }
-            if (zeroed) fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPFull + x));
