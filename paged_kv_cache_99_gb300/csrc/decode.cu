@@ -974,16 +974,12 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, int u, const
 // past its prologue, while the decode grid drains.  For batches of up to kCombineScanSeqs sequences every CTA first builds the
 // exclusive block prefix over the sequences in shared memory, overlapping the
 // decode grid's tail; the units it then visits only look it up.
-template <bool OutBf16, bool Fp8Layout, bool Cascade, int kBatch>
-__global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
-    __shared__ int pre_sum[kCombineScanSeqs + 1];
-    __shared__ int warp_sum[8];
-    // a launch chained behind (the next layer's decode) may become resident now and
-    // wait for this grid's completion with its prologue done
-    grid_launch_dependents();
+// The exclusive block prefix over the sequences (batches of up to kCombineScanSeqs),
+// by a 256-thread CTA into shared memory.
+__device__ __forceinline__ void combine_block_prefix(const DecodeParams& p, int* pre_sum, int* warp_sum) {
     const int B = p.num_seqs;
     const int UH = p.num_kv_heads * p.head_groups;
-    if (B <= kCombineScanSeqs) {
+    {
         // thread i sums sequences [per i, per (i + 1)), then a scan over threads
         const int per = (B + 255) / 256;
         const int beg = min(B, static_cast<int>(threadIdx.x) * per), end = min(B, beg + per);
@@ -1008,6 +1004,18 @@ __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
         if (threadIdx.x == 255) pre_sum[B] = before + inc;
         __syncthreads();
     }
+}
+
+template <bool OutBf16, bool Fp8Layout, bool Cascade, int kBatch>
+__global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
+    __shared__ int pre_sum[kCombineScanSeqs + 1];
+    __shared__ int warp_sum[8];
+    // a launch chained behind (the next layer's decode) may become resident now and
+    // wait for this grid's completion with its prologue done
+    grid_launch_dependents();
+    const int B = p.num_seqs;
+    const int UH = p.num_kv_heads * p.head_groups;
+    if (B <= kCombineScanSeqs) combine_block_prefix(p, pre_sum, warp_sum);
     const long long units = static_cast<long long>(B) * UH;
     for (long long u = blockIdx.x; u < units; u += gridDim.x)
         combine_unit<OutBf16, Fp8Layout, Cascade, kBatch>(p, static_cast<int>(u), pre_sum);
@@ -1016,6 +1024,161 @@ __global__ void __maxnreg__(112) combine_kernel(const DecodeParams p) {
         grid_dependency_wait();
         p.claim[1] = __ldcg(p.claim);
     }
+}
+
+// Cascade combine, one warp per unit: every row of a cascade has a shared-prefix
+// partial, so every unit is merged, and with many units a CTA per unit would run
+// them in rounds.  A lane holds the fragments of heads 2t, 2t+1 in all eight
+// 16-wide slices of d; partials are folded one per round trip.
+template <bool OutBf16, bool Fp8Layout>
+__device__ __forceinline__ void combine_unit_warp(const DecodeParams& p, int u, const int* pre_sum) {
+    const int UH = p.num_kv_heads * p.head_groups;
+    const int s = u / UH, uh = u % UH;
+    const int B = p.num_seqs;
+    const int lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
+    long long lo = 0, T = 0;
+    if (B <= kCombineScanSeqs) {
+        lo = pre_sum[s];
+        T = pre_sum[B];
+    } else {
+        grid_dependency_wait();
+        lo = p.plan[s];
+        T = p.plan[B];
+    }
+    const int nb = unit_blocks_of(p, s, UH) / UH;
+    // the unit's decode partials (static ranges merged per CTA, as in combine_unit)
+    int wa = 0, wb = 0, nseg = 0, m0 = 0;
+    if (nb > 0 && T > 0) {
+        const Split sp = make_split(static_cast<int>(T), p.num_workers, p.dyn256);
+        const int fu = static_cast<int>(lo) + uh * nb;
+        wa = sp.range_of(fu);
+        wb = sp.range_of(fu + nb - 1);
+        if (wa == wb) {
+            nseg = 1;
+        } else {
+            m0 = (wa / kDecodeWarps + 1) * kDecodeWarps;
+            nseg = 2 + (m0 <= wb - 1 ? (wb - 1 - m0) / kDecodeWarps + 1 : 0);
+        }
+    }
+    const int npre = p.first_block > 0 ? p.prefix_splits : 0;
+    if (nseg + npre == 0) return;     // an empty row: the decode grid wrote its zeros
+    const int h = uh / p.head_groups, hg = uh % p.head_groups;
+    const int row = p.query_start_loc ? p.query_start_loc[s] : s;
+    const size_t rows = static_cast<size_t>(B) * p.num_q_heads;
+    auto range_k = [&](int k) -> int {
+        if (wa == wb) return wa;
+        return k == 0 ? wa : (k == nseg - 1 ? wb : m0 + kDecodeWarps * (k - 1));
+    };
+    // partial k: the prefix segments first, then the decode slots
+    auto load = [&](int k, float (&v)[8][4], float& ma, float& mb, float& la, float& lb) {
+        if (k < npre) {
+            const float* so = k == 0 ? p.prefix_o : p.prefix_o_extra + (k - 1) * rows * kHeadDim;
+            const float* sm = k == 0 ? p.prefix_ml : p.prefix_ml_extra + (k - 1) * rows * 2;
+            float mm[2] = {-INFINITY, -INFINITY}, ll[2] = {0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int gh = hg * kHeadsPerGroup + 2 * t + e;
+                const bool live = gh < p.group;
+                const size_t ri = static_cast<size_t>(row) * p.num_q_heads + h * p.group + (live ? gh : 0);
+                if (live) {
+                    const float2 ml2 = __ldcg(reinterpret_cast<const float2*>(sm + 2 * ri));
+                    mm[e] = ml2.x;
+                    ll[e] = ml2.y;
+                }
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    const int dA = Fp8Layout ? 16 * dt + 2 * g : 16 * dt + g;
+                    const int dB = Fp8Layout ? dA + 1 : dA + 8;
+                    v[dt][e] = live ? __ldcg(so + ri * kHeadDim + dA) : 0.f;
+                    v[dt][2 + e] = live ? __ldcg(so + ri * kHeadDim + dB) : 0.f;
+                }
+            }
+            ma = mm[0];
+            mb = mm[1];
+            la = ll[0];
+            lb = ll[1];
+        } else {
+            const size_t sl = static_cast<size_t>(range_k(k - npre)) + u;
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                const float4 x = __ldcg(p.partial + (sl * 8 + dt) * 32 + lane);
+                v[dt][0] = x.x;
+                v[dt][1] = x.y;
+                v[dt][2] = x.z;
+                v[dt][3] = x.w;
+            }
+            const float2 mv = __ldcg(reinterpret_cast<const float2*>(p.ml + sl * 16 + 2 * t));
+            const float2 lv = __ldcg(reinterpret_cast<const float2*>(p.ml + sl * 16 + 8 + 2 * t));
+            ma = mv.x;
+            mb = mv.y;
+            la = lv.x;
+            lb = lv.y;
+        }
+    };
+    if (B <= kCombineScanSeqs) grid_dependency_wait();
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float acc[8][4];
+#pragma unroll
+    for (int dt = 0; dt < 8; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+    // fold one partial into the running (M, L, acc) (padding heads may turn to NaN: never written)
+    auto fold = [&](const float (&v)[8][4], float ma, float mb, float la, float lb) {
+        const float n0 = fmaxf(M0, ma), n1 = fmaxf(M1, mb);
+        const float r0 = exp2f(M0 - n0), r1 = exp2f(M1 - n1);      // 0 while nothing is summed
+        const float w0 = exp2f(ma - n0), w1 = exp2f(mb - n1);
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+            acc[dt][0] = acc[dt][0] * r0 + v[dt][0] * w0;
+            acc[dt][1] = acc[dt][1] * r1 + v[dt][1] * w1;
+            acc[dt][2] = acc[dt][2] * r0 + v[dt][2] * w0;
+            acc[dt][3] = acc[dt][3] * r1 + v[dt][3] * w1;
+        }
+        L0 = L0 * r0 + la * w0;
+        L1 = L1 * r1 + lb * w1;
+        M0 = n0;
+        M1 = n1;
+    };
+    const int nall = npre + nseg;
+    for (int k = 0; k < nall; ++k) {
+        float v[8][4];
+        float ma, mb, la, lb;
+        load(k, v, ma, mb, la, lb);
+        fold(v, ma, mb, la, lb);
+    }
+    const float vscale = Fp8Layout ? __ldg(p.v_scale + h * p.scale_stride) : 1.0f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int gh = hg * kHeadsPerGroup + 2 * t + e;
+        if (gh >= p.group) continue;
+        const float inv = vscale / (e ? L1 : L0);
+        uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                         (static_cast<size_t>(row) * p.num_q_heads + h * p.group + gh) * kHeadDim;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+            const uint16_t lo16 = from_float<OutBf16>(acc[dt][e] * inv);
+            const uint16_t hi16 = from_float<OutBf16>(acc[dt][2 + e] * inv);
+            if constexpr (Fp8Layout) {
+                *reinterpret_cast<uint32_t*>(orow + 16 * dt + 2 * g) =
+                    static_cast<uint32_t>(lo16) | (static_cast<uint32_t>(hi16) << 16);
+            } else {
+                orow[16 * dt + g] = lo16;
+                orow[16 * dt + g + 8] = hi16;
+            }
+        }
+    }
+}
+
+// 8 units per 256-thread CTA, one per warp.  At most 112 registers, as combine_kernel.
+template <bool OutBf16, bool Fp8Layout>
+__global__ void __maxnreg__(112) combine_cascade_kernel(const DecodeParams p) {
+    __shared__ int pre_sum[kCombineScanSeqs + 1];
+    __shared__ int warp_sum[8];
+    grid_launch_dependents();
+    const int B = p.num_seqs;
+    const int UH = p.num_kv_heads * p.head_groups;
+    if (B <= kCombineScanSeqs) combine_block_prefix(p, pre_sum, warp_sum);
+    const long long units = static_cast<long long>(B) * UH;
+    const long long u = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (u < units) combine_unit_warp<OutBf16, Fp8Layout>(p, static_cast<int>(u), pre_sum);
 }
 
 // ---------------------------------------------------------------------------
@@ -1097,7 +1260,11 @@ cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p,
                            cudaStream_t stream) {
     const long long units = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.head_groups;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(units < max_ctas ? units : max_ctas));
+    // a cascade with more units than resident combine CTAs: one warp per unit, 8 units
+    // per CTA (a CTA per unit would take them in rounds); with fewer units a CTA per unit
+    // batches a unit's partials (the prefix segments of a long prompt) in one round trip
+    const bool warp_units = p.cascade && units > max_ctas;
+    cfg.gridDim = dim3(static_cast<unsigned>(warp_units ? (units + 7) / 8 : (units < max_ctas ? units : max_ctas)));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1114,6 +1281,7 @@ cudaError_t launch_combine(bool out_bf16, bool fp8_cache, const DecodeParams& p,
     const bool wide = !p.cascade && static_cast<long long>(p.num_workers) > per_slot * units;
     auto kernel = [&](auto ob, auto f8) -> const void* {
         constexpr bool O = decltype(ob)::value, F = decltype(f8)::value;
+        if (warp_units) return reinterpret_cast<const void*>(&combine_cascade_kernel<O, F>);
         if (p.cascade) return reinterpret_cast<const void*>(&combine_kernel<O, F, true, 8>);
         return wide ? reinterpret_cast<const void*>(&combine_kernel<O, F, false, 10>)
                     : reinterpret_cast<const void*>(&combine_kernel<O, F, false, 8>);

@@ -180,3 +180,23 @@ def test_cascade_split_long_prefix_sampled():
     pick = sorted({0, 1, int(lens.argmax()), int(lens.argmin()), w.num_seqs // 2, w.num_seqs - 1})
     rows, ref = oracle_step(w, 0, pick)
     compare(out, rows, ref, "long shared prefix, split, sampled rows")
+
+
+# ---- more (sequence, KV head) units than resident combine CTAs: one warp merges a unit ----
+
+@pytest.mark.parametrize("cache,qd,G", [("bf16", "bf16", 4), ("fp8", "bf16", 8), ("fp16", "fp16", 12)])
+@pytest.mark.parametrize("prefix,split", [(6, False), (40, True)])
+def test_cascade_many_units_warp_merge(cache, qd, G, prefix, split):
+    # 96 sequences x 8 KV heads (x 2 head groups for G = 12): 768 or 1536 units, more
+    # than two combine CTAs per SM; every suffix length class, the prefix whole (6
+    # blocks) or cut into key segments (40 blocks = 640 keys with the split workspace)
+    g = np.random.default_rng(prefix + G)
+    suffixes = (SUFFIXES * 14)[:96]
+    suffixes = [int(x) for x in g.permutation(suffixes)]
+    w = _case(97 + G + prefix, prefix, suffixes, G, Hkv=8, cache=cache, qd=qd)
+    assert w.num_seqs * w.num_kv_heads > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    out, st = _cascade(w, prefix, ws=_split_ws(w) if split else None)
+    assert st == pa.PA_OK, pa.pa_status_string(st)
+    pick = sorted({0, 1, 2, 3, 5, 6, 47, 94, 95} | {int(i) for i in g.choice(96, 6, replace=False)})
+    rows, ref = oracle_step(w, 0, pick)
+    compare(out, rows, ref, f"cascade warp merge {cache} G={G} prefix={prefix}")
