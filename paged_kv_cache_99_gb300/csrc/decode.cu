@@ -1046,15 +1046,17 @@ __device__ __forceinline__ void combine_unit_warp(const DecodeParams& p, int u, 
         T = p.plan[B];
     }
     const int nb = unit_blocks_of(p, s, UH) / UH;
-    // the unit's decode partials (static ranges merged per CTA, as in combine_unit)
+    // the unit's decode partials, as in combine_unit: one per range, or with static
+    // ranges one per CTA run of the ranges it spans
     int wa = 0, wb = 0, nseg = 0, m0 = 0;
+    const bool cta_merged = p.dyn256 == 0;
     if (nb > 0 && T > 0) {
         const Split sp = make_split(static_cast<int>(T), p.num_workers, p.dyn256);
         const int fu = static_cast<int>(lo) + uh * nb;
         wa = sp.range_of(fu);
         wb = sp.range_of(fu + nb - 1);
-        if (wa == wb) {
-            nseg = 1;
+        if (!cta_merged || wa == wb) {
+            nseg = wb - wa + 1;
         } else {
             m0 = (wa / kDecodeWarps + 1) * kDecodeWarps;
             nseg = 2 + (m0 <= wb - 1 ? (wb - 1 - m0) / kDecodeWarps + 1 : 0);
@@ -1066,7 +1068,7 @@ __device__ __forceinline__ void combine_unit_warp(const DecodeParams& p, int u, 
     const int row = p.query_start_loc ? p.query_start_loc[s] : s;
     const size_t rows = static_cast<size_t>(B) * p.num_q_heads;
     auto range_k = [&](int k) -> int {
-        if (wa == wb) return wa;
+        if (!cta_merged || wa == wb) return wa + k;
         return k == 0 ? wa : (k == nseg - 1 ? wb : m0 + kDecodeWarps * (k - 1));
     };
     // partial k: the prefix segments first, then the decode slots
