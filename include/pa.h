@@ -149,7 +149,10 @@ PA_API size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  */
 PA_API size_t pa_workspace_size_shared_prefix(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
 
-/* Default number of decode workers (warps) on the current device. */
+/* Default number of decode workers (warps) on the current device for a 16-bit
+ * cache: two 4-warp CTAs per SM.  An FP8 cache defaults to twice as many (four
+ * CTAs per SM: its warps are bound by the latency of the work on each block, not
+ * by HBM).  Explicit worker counts run from 1 to this value for either. */
 PA_API int pa_default_workers(void);
 
 /*

@@ -43,7 +43,7 @@ struct DecodeCfg {
     static constexpr bool kFp8 = Kind == kKindFp8;
     static constexpr int kTileBytes = kFp8 ? 2048 : 4096;   // one (block, head) tile
     static constexpr int kStageBytes = 2 * kTileBytes;      // K then V
-    static constexpr int kStages = kFp8 ? 6 : 3;
+    static constexpr int kStages = 3;                        // per warp
     static constexpr int kTileArea = kDecodeWarps * kStages * kStageBytes;
     static constexpr int kBarBytes = kDecodeWarps * kStages * 8;
 };
@@ -783,11 +783,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
     }
 }
 
-// At most 136 registers per thread: two CTAs (128 threads each) and a combine CTA
-// (256 threads, at most 112) share an SM, so the combine is resident, past its
-// prologue, while the decode grid drains.
+// 16-bit caches: at most 136 registers per thread, so that two CTAs (128 threads
+// each) and a combine CTA (256 threads, at most 112) share an SM and the combine is
+// resident, past its prologue, while the decode grid drains.  FP8 caches: 128, so
+// that four CTAs fill the register file.
+template <int Kind>
+constexpr int decode_max_regs() { return Kind == kKindFp8 ? 128 : 136; }
+
 template <int Kind, bool QBf16, bool Dyn>
-__global__ void __maxnreg__(136)
+__global__ void __maxnreg__(decode_max_regs<Kind>())
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
     decode_body<Kind, QBf16, false, Dyn>(kmap, vmap, p);
@@ -800,7 +804,7 @@ __global__ void __maxnreg__(136)
 
 // The same with the new tokens' slot write fused in (pa_decode_append).
 template <int Kind, bool QBf16, bool Dyn>
-__global__ void __maxnreg__(136)
+__global__ void __maxnreg__(decode_max_regs<Kind>())
     decode_append_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                          const DecodeParams p) {
     decode_body<Kind, QBf16, true, Dyn>(kmap, vmap, p);

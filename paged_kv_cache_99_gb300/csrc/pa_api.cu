@@ -223,12 +223,14 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
             ctas = it->second;
         }
     }
-    ctas = ctas > kMaxDecodeCtasPerSm ? kMaxDecodeCtasPerSm : ctas;
+    const int cap = kind == kKindFp8 ? kMaxDecodeCtasPerSmFp8 : kMaxDecodeCtasPerSm;
+    ctas = ctas > cap ? cap : ctas;
     const int full = st->sms * ctas * kDecodeWarps;
     if (num_workers < 0 || num_workers > max_workers(*st)) return PA_ERR_INVALID_ARG;
     const int W = num_workers == 0 ? full : num_workers;
     const int hg = head_groups_of(num_q_heads, num_kv_heads);
-    const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, hg, W);
+    // one slot per static range, and as many for claimed pieces
+    const WorkspaceLayout lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, hg, dyn ? 2 * W : W);
     if (workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
 
     CUtensorMap kmap, vmap;
@@ -355,11 +357,11 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
 }  // namespace
 
 WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_groups,
-                                        int workers) {
+                                        int range_slots) {
     WorkspaceLayout l;
     const size_t units = static_cast<size_t>(num_seqs) * num_kv_heads * head_groups;
-    // ranges: one static range per worker and at most as many claimed pieces
-    const size_t slots = units + 2 * static_cast<size_t>(workers);
+    // a range's partial of unit u sits in slot (range index + u)
+    const size_t slots = units + static_cast<size_t>(range_slots);
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
     l.status_off = 0;
     l.plan_off = 256;
@@ -474,8 +476,10 @@ size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int he
         return 0;
     DeviceState* st = device_state(nullptr);
     if (!st) return 0;
+    // the most range slots a call takes: a 16-bit grid's workers and as many claimed
+    // pieces, or an FP8 grid's (twice as many) workers
     return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_groups_of(num_q_heads, num_kv_heads),
-                                   max_workers(*st))
+                                   2 * max_workers(*st))
         .total;
 }
 
@@ -678,7 +682,7 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
     if (num_seqs == 0) return PA_OK;
     // the largest worker count this device can use bounds the scratch a call needs
     const size_t need = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads,
-                                                head_groups_of(num_q_heads, num_kv_heads), max_workers(*st)).total;
+                                                head_groups_of(num_q_heads, num_kv_heads), 2 * max_workers(*st)).total;
     if (need > kNoAllocScratchBytes) {
         snprintf(g_last_error, sizeof g_last_error,
                  "pa_decode_noalloc: this batch needs %zu bytes of scratch; the static scratch holds %zu",

@@ -16,7 +16,12 @@ constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;
 constexpr int kMaxSeqs = 8192;
 constexpr int kDecodeWarps = 4;        // warps per decode CTA
-constexpr int kMaxDecodeCtasPerSm = 2;
+constexpr int kMaxDecodeCtasPerSm = 2;     // 16-bit caches: their rings fill shared memory
+// FP8 caches: four CTAs (three stages each) fill the register file.  An FP8 warp is
+// bound by the latency of the work on each block, not by HBM, so more warps per SM
+// stream faster; its ranges need no claimed pieces, so its 2x workers fit the same
+// partial slots as the 16-bit grid's workers and pieces.
+constexpr int kMaxDecodeCtasPerSmFp8 = 4;
 // Decode work claimed at run time: this share (in 1/256) of the flattened blocks
 // goes to pieces of at least kMinPiece blocks (more than a ring holds) when static
 // ranges hold at least kMinPieceRange blocks; a claim is sent kClaimAhead blocks
@@ -149,8 +154,10 @@ struct WorkspaceLayout {
     size_t total;
 };
 
+// range_slots: partial slots besides one per unit (one per static range, plus one per
+// claimed piece when pieces are on)
 WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_groups,
-                                        int slots_workers);
+                                        int range_slots);
 
 // Decode kernels: dynamic shared memory for num_seqs sequences.
 size_t decode_smem_bytes(CacheKind kind, int num_seqs);
