@@ -521,13 +521,17 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         const int pos = live ? qpos(jf + jq) : qpos(jl);
         const size_t qrow = (static_cast<size_t>(q0 + (live ? jf + jq : jf0)) * p.num_q_heads + h * G +
                              (live ? r % G : 0)) * kHeadDim;
-        // Q row -> shared memory (MMA input type), 128-byte swizzle, two d-halves
+        // Q row -> shared memory (MMA input type), 128-byte swizzle, two d-halves; the
+        // row's 16 loads all go out before the first store (one memory round trip)
         {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qrow);
             uint8_t* qdst = sm + kOffQ + x * 2 * kQHalf;
-#pragma unroll 4
+            uint4 qv[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) qv[c] = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
             for (int c = 0; c < 16; ++c) {
-                uint4 v = live ? src[c] : make_uint4(0, 0, 0, 0);
+                uint4 v = qv[c];
                 if constexpr (kFp8 && QBf16) {
                     uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
