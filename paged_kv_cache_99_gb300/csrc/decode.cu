@@ -1185,6 +1185,11 @@ __global__ void __maxnreg__(112) combine_cascade_kernel(const DecodeParams p) {
     const long long units = static_cast<long long>(B) * UH;
     const long long u = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (u < units) combine_unit_warp<OutBf16, Fp8Layout>(p, static_cast<int>(u), pre_sum);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        // every claim of this call is made: the next call numbers its pieces from here
+        grid_dependency_wait();
+        p.claim[1] = __ldcg(p.claim);
+    }
 }
 
 // ---------------------------------------------------------------------------

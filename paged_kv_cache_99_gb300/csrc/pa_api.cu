@@ -189,9 +189,10 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     // workers' ranges are long (judged from the table width: the decode grid decides
     // from the lengths) and the warps keep HBM busy: FP8 warps, and 16-bit warps with
     // more than 4 query heads per unit, are bound by the latency of each block, not
-    // by HBM, and lose more to the pieces than the balance gains.  A mixed batch's decode grid starts beside the chunk grid, CTA
-    // by CTA, and a cascade's beside the prefix grid, whose end it rarely sets: both
-    // keep static ranges
+    // by HBM, and lose more to the pieces than the balance gains.  A mixed batch's
+    // decode grid starts beside the chunk grid, CTA by CTA, and keeps static ranges; a
+    // cascade's takes the SMs the prefix grid leaves free from the start and claims
+    // like a plain decode
     const int hg0 = head_groups_of(num_q_heads, num_kv_heads);
     const long long units_max = static_cast<long long>(num_seqs) * num_kv_heads * hg0;
     const long long per_unit_max = (static_cast<long long>(max_blocks_per_seq) * block_size + kBlockSize - 1) / kBlockSize;
@@ -199,7 +200,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     const int w_default = st->sms * kMaxDecodeCtasPerSm * kDecodeWarps;
     const int w_est = num_workers > 0 ? num_workers : w_default;
     const int unit_heads = num_q_heads / num_kv_heads < kHeadsPerGroup ? num_q_heads / num_kv_heads : kHeadsPerGroup;
-    const bool dyn = query_start_loc == nullptr && !cascade && kind != kKindFp8 && unit_heads <= 4 &&
+    const bool dyn = query_start_loc == nullptr && kind != kKindFp8 && unit_heads <= 4 &&
                      t_max / w_est >= kMinPieceRange;
     const size_t smem = decode_smem_bytes(kind, num_seqs);
     if (smem + 1024 > st->max_smem_optin) return PA_ERR_UNSUPPORTED;

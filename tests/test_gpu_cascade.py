@@ -200,3 +200,28 @@ def test_cascade_many_units_warp_merge(cache, qd, G, prefix, split):
     pick = sorted({0, 1, 2, 3, 5, 6, 47, 94, 95} | {int(i) for i in g.choice(96, 6, replace=False)})
     rows, ref = oracle_step(w, 0, pick)
     compare(out, rows, ref, f"cascade warp merge {cache} G={G} prefix={prefix}")
+
+
+def test_cascade_claimed_pieces_consecutive_calls():
+    # units of 4 query heads over long private suffixes: the suffix decode hands out
+    # its last pieces from the workspace counter, and the warp merge (more units than
+    # combine CTAs) leaves the counter's base for the next call; three calls on one
+    # workspace, then a plain decode and one more cascade, each against the oracle
+    g = np.random.default_rng(7)
+    suffixes = [int(x) for x in g.integers(1500, 2600, 96)]
+    w = _case(131, 6, suffixes, 4, Hkv=8)
+    assert w.num_seqs * w.num_kv_heads > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    pick = sorted({0, 1, 47, 94, 95} | {int(i) for i in g.choice(96, 5, replace=False)})
+    rows, ref = oracle_step(w, 0, pick)
+    ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads)
+    for i in range(3):
+        out, st = _cascade(w, 6, ws=ws)
+        assert st == pa.PA_OK, pa.pa_status_string(st)
+        compare(out, rows, ref, f"cascade call {i}")
+    dec = torch.empty_like(w.q[0])
+    pa.pa_decode(dec, w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables, w.seq_lens, w.scale, ws)
+    torch.cuda.synchronize()
+    compare(dec, rows, ref, "plain decode in between")
+    out, st = _cascade(w, 6, ws=ws)
+    assert st == pa.PA_OK
+    compare(out, rows, ref, "cascade after the decode")
