@@ -38,12 +38,12 @@ namespace pa {
 
 namespace {
 
-template <int Kind>
+template <int Kind, int Stages = 3>
 struct DecodeCfg {
     static constexpr bool kFp8 = Kind == kKindFp8;
     static constexpr int kTileBytes = kFp8 ? 2048 : 4096;   // one (block, head) tile
     static constexpr int kStageBytes = 2 * kTileBytes;      // K then V
-    static constexpr int kStages = 3;                        // per warp
+    static constexpr int kStages = Stages;                   // per warp
     static constexpr int kTileArea = kDecodeWarps * kStages * kStageBytes;
     static constexpr int kBarBytes = kDecodeWarps * kStages * 8;
 };
@@ -151,9 +151,9 @@ __device__ __forceinline__ T shfl(T v, int src) {
 
 }  // namespace
 
-template <int Kind, bool QBf16, bool Append, bool Dyn>
+template <int Kind, bool QBf16, bool Append, bool Dyn, int Stages = 3>
 __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p) {
-    using Cfg = DecodeCfg<Kind>;
+    using Cfg = DecodeCfg<Kind, Stages>;
     constexpr bool kFp8 = Cfg::kFp8;
     constexpr bool kMmaBf16 = Kind == kKindBf16;   // fp16 and FP8 (widened) use f16 MMA
     constexpr int NS = Cfg::kStages;
@@ -785,16 +785,17 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kmap, const CUten
 
 // 16-bit caches: at most 136 registers per thread, so that two CTAs (128 threads
 // each) and a combine CTA (256 threads, at most 112) share an SM and the combine is
-// resident, past its prologue, while the decode grid drains.  FP8 caches: 128, so
-// that four CTAs fill the register file.
+// resident, past its prologue, while the decode grid drains (with the two-stage
+// ring, three CTAs per SM and the combine starts as they drain).  FP8 caches: 128,
+// so that four CTAs fill the register file.
 template <int Kind>
 constexpr int decode_max_regs() { return Kind == kKindFp8 ? 128 : 136; }
 
-template <int Kind, bool QBf16, bool Dyn>
+template <int Kind, bool QBf16, bool Dyn, int Stages>
 __global__ void __maxnreg__(decode_max_regs<Kind>())
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
-    decode_body<Kind, QBf16, false, Dyn>(kmap, vmap, p);
+    decode_body<Kind, QBf16, false, Dyn, Stages>(kmap, vmap, p);
     // Overlapping a chunk launch of the same call (which neither reads what this grid
     // writes nor writes what it reads): the last CTA alone waits for it before exiting,
     // so that this grid, and the combine chained behind it, completes after it while
@@ -1197,55 +1198,67 @@ __global__ void __maxnreg__(112) combine_cascade_kernel(const DecodeParams p) {
 // ---------------------------------------------------------------------------
 
 namespace {
+// narrow: the two-stage ring of the 16-bit decode kernel (no fused slot write)
 template <int Kind, bool QBf16>
-void* kernel_ptr(bool append, bool dyn) {
+void* kernel_ptr(bool append, bool dyn, bool narrow) {
+    if constexpr (Kind != kKindFp8) {
+        if (narrow && !append)
+            return dyn ? reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, true, 2>)
+                       : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, false, 2>);
+    }
     if (dyn)
         return append ? reinterpret_cast<void*>(&decode_append_kernel<Kind, QBf16, true>)
-                      : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, true>);
+                      : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, true, 3>);
     return append ? reinterpret_cast<void*>(&decode_append_kernel<Kind, QBf16, false>)
-                  : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, false>);
+                  : reinterpret_cast<void*>(&decode_kernel<Kind, QBf16, false, 3>);
 }
 
-void* decode_fn(CacheKind kind, bool q_bf16, bool append, bool dyn) {
+void* decode_fn(CacheKind kind, bool q_bf16, bool append, bool dyn, bool narrow) {
     switch (kind) {
-        case kKindBf16: return kernel_ptr<kKindBf16, true>(append, dyn);
-        case kKindFp16: return kernel_ptr<kKindFp16, false>(append, dyn);
+        case kKindBf16: return kernel_ptr<kKindBf16, true>(append, dyn, narrow);
+        case kKindFp16: return kernel_ptr<kKindFp16, false>(append, dyn, narrow);
         case kKindFp8:
-            return q_bf16 ? kernel_ptr<kKindFp8, true>(append, dyn) : kernel_ptr<kKindFp8, false>(append, dyn);
+            return q_bf16 ? kernel_ptr<kKindFp8, true>(append, dyn, false)
+                          : kernel_ptr<kKindFp8, false>(append, dyn, false);
     }
     return nullptr;
 }
 
-int tile_area_bytes(CacheKind kind) {
+int tile_area_bytes(CacheKind kind, bool narrow) {
     switch (kind) {
-        case kKindBf16: return DecodeCfg<kKindBf16>::kTileArea + DecodeCfg<kKindBf16>::kBarBytes;
-        case kKindFp16: return DecodeCfg<kKindFp16>::kTileArea + DecodeCfg<kKindFp16>::kBarBytes;
+        case kKindBf16:
+            return narrow ? DecodeCfg<kKindBf16, 2>::kTileArea + DecodeCfg<kKindBf16, 2>::kBarBytes
+                          : DecodeCfg<kKindBf16>::kTileArea + DecodeCfg<kKindBf16>::kBarBytes;
+        case kKindFp16:
+            return narrow ? DecodeCfg<kKindFp16, 2>::kTileArea + DecodeCfg<kKindFp16, 2>::kBarBytes
+                          : DecodeCfg<kKindFp16>::kTileArea + DecodeCfg<kKindFp16>::kBarBytes;
         case kKindFp8: return DecodeCfg<kKindFp8>::kTileArea + DecodeCfg<kKindFp8>::kBarBytes;
     }
     return 0;
 }
 }  // namespace
 
-size_t decode_smem_bytes(CacheKind kind, int num_seqs) {
+size_t decode_smem_bytes(CacheKind kind, int num_seqs, bool narrow) {
     // 1 KiB alignment slack + tiles + barriers + scan array
-    return 1024 + static_cast<size_t>(tile_area_bytes(kind)) + static_cast<size_t>(num_seqs + 1) * 4;
+    return 1024 + static_cast<size_t>(tile_area_bytes(kind, narrow)) + static_cast<size_t>(num_seqs + 1) * 4;
 }
 
-cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t max_smem) {
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, bool dyn, bool narrow, size_t max_smem) {
     // the largest request a call can make (kMaxSeqs sequences), within what the
     // device allows next to the kernel's static shared memory
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, decode_fn(kind, q_bf16, append, dyn));
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_fn(kind, q_bf16, append, dyn, narrow));
     if (e != cudaSuccess) return e;
-    size_t want = decode_smem_bytes(kind, kMaxSeqs);
+    size_t want = decode_smem_bytes(kind, kMaxSeqs, narrow);
     const size_t cap = max_smem > fa.sharedSizeBytes ? max_smem - fa.sharedSizeBytes : 0;
     if (want > cap) want = cap;
-    return cudaFuncSetAttribute(decode_fn(kind, q_bf16, append, dyn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(want));
+    return cudaFuncSetAttribute(decode_fn(kind, q_bf16, append, dyn, narrow),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(want));
 }
 
-cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t smem, int* ctas_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_fn(kind, q_bf16, append, dyn),
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, bool dyn, bool narrow, size_t smem,
+                             int* ctas_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_fn(kind, q_bf16, append, dyn, narrow),
                                                          kDecodeWarps * 32, smem);
 }
 
@@ -1262,7 +1275,7 @@ cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     void* args[] = {const_cast<CUtensorMap*>(&kmap), const_cast<CUtensorMap*>(&vmap), const_cast<DecodeParams*>(&p)};
-    const void* fn = decode_fn(kind, q_bf16, p.append != 0, p.dyn256 > 0);
+    const void* fn = decode_fn(kind, q_bf16, p.append != 0, p.dyn256 > 0, p.narrow != 0);
     if (!fn) return cudaErrorInvalidValue;
     return cudaLaunchKernelExC(&cfg, fn, args);
 }

@@ -24,7 +24,7 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     size_t max_smem_optin = 0;
-    bool decode_prepared[3][2][2][2] = {};
+    bool decode_prepared[3][2][2][2][2] = {};
     bool chunk_prepared[3][2] = {};
 };
 
@@ -202,21 +202,24 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     const int unit_heads = num_q_heads / num_kv_heads < kHeadsPerGroup ? num_q_heads / num_kv_heads : kHeadsPerGroup;
     const bool dyn = query_start_loc == nullptr && kind != kKindFp8 && unit_heads <= 4 &&
                      t_max / w_est >= kMinPieceRange;
-    const size_t smem = decode_smem_bytes(kind, num_seqs);
+    // a cascade's suffix decode and a mixed batch's decode rows (16-bit caches) take
+    // the two-stage ring and three CTAs per SM
+    const bool narrow = kind != kKindFp8 && !append && (cascade || query_start_loc != nullptr);
+    const size_t smem = decode_smem_bytes(kind, num_seqs, narrow);
     if (smem + 1024 > st->max_smem_optin) return PA_ERR_UNSUPPORTED;
     int ctas = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!st->decode_prepared[kind][q_bf16][append][dyn]) {
-            cudaError_t e = decode_prepare(kind, q_bf16, append, dyn, st->max_smem_optin);
+        if (!st->decode_prepared[kind][q_bf16][append][dyn][narrow]) {
+            cudaError_t e = decode_prepare(kind, q_bf16, append, dyn, narrow, st->max_smem_optin);
             if (e != cudaSuccess) return fail("cudaFuncSetAttribute(decode)", e);
-            st->decode_prepared[kind][q_bf16][append][dyn] = true;
+            st->decode_prepared[kind][q_bf16][append][dyn][narrow] = true;
         }
         auto key = std::make_tuple(dev, static_cast<int>(kind), static_cast<int>(q_bf16), static_cast<int>(append),
-                                   static_cast<int>(dyn), smem);
+                                   static_cast<int>(dyn) + 2 * static_cast<int>(narrow), smem);
         auto it = g_occupancy.find(key);
         if (it == g_occupancy.end()) {
-            cudaError_t e = decode_occupancy(kind, q_bf16, append, dyn, smem, &ctas);
+            cudaError_t e = decode_occupancy(kind, q_bf16, append, dyn, narrow, smem, &ctas);
             if (e != cudaSuccess) return fail("cudaOccupancyMaxActiveBlocksPerMultiprocessor(decode)", e);
             if (ctas <= 0) return fail_msg("decode kernel does not fit on an SM");
             g_occupancy[key] = ctas;
@@ -224,7 +227,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
             ctas = it->second;
         }
     }
-    const int cap = kind == kKindFp8 ? kMaxDecodeCtasPerSmFp8 : kMaxDecodeCtasPerSm;
+    const int cap = kind == kKindFp8 ? kMaxDecodeCtasPerSmFp8 : narrow ? kMaxDecodeCtasPerSmNarrow : kMaxDecodeCtasPerSm;
     ctas = ctas > cap ? cap : ctas;
     const int full = st->sms * ctas * kDecodeWarps;
     if (num_workers < 0 || num_workers > max_workers(*st)) return PA_ERR_INVALID_ARG;
@@ -266,6 +269,7 @@ pa_status decode_impl(void* out, const void* q, const int32_t* query_start_loc, 
     p.block_shift = block_shift_of(block_size);
     p.num_workers = W;
     p.dyn256 = dyn ? kDynShare256 : 0;
+    p.narrow = narrow ? 1 : 0;
     p.claim = reinterpret_cast<unsigned*>(ws + lay.status_off + 8);
     p.overlap_prior = overlap_prior ? 1 : 0;
     p.cascade = cascade ? 1 : 0;
@@ -477,10 +481,11 @@ size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int he
         return 0;
     DeviceState* st = device_state(nullptr);
     if (!st) return 0;
-    // the most range slots a call takes: a 16-bit grid's workers and as many claimed
-    // pieces, or an FP8 grid's (twice as many) workers
+    // the most range slots a call takes: a two-stage 16-bit grid's workers (three
+    // CTAs per SM) and as many claimed pieces (an FP8 grid's workers, or a plain
+    // 16-bit grid's workers and pieces, take fewer)
     return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_groups_of(num_q_heads, num_kv_heads),
-                                   2 * max_workers(*st))
+                                   2 * st->sms * kMaxDecodeCtasPerSmNarrow * kDecodeWarps)
         .total;
 }
 

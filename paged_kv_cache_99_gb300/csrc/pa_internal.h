@@ -22,6 +22,12 @@ constexpr int kMaxDecodeCtasPerSm = 2;     // 16-bit caches: their rings fill sh
 // stream faster; its ranges need no claimed pieces, so its 2x workers fit the same
 // partial slots as the 16-bit grid's workers and pieces.
 constexpr int kMaxDecodeCtasPerSmFp8 = 4;
+// 16-bit caches in a cascade's suffix decode or a mixed batch's decode rows: a
+// two-stage ring per warp and three CTAs per SM.  More warps hide the work on each
+// block (those grids run beside another grid and their rows are short or come from
+// L2); for a plain decode from HBM the deeper ring streams faster.  Their workers and
+// pieces take at most 2 x SMs x 3 x 4 partial slots, which pa_workspace_size covers.
+constexpr int kMaxDecodeCtasPerSmNarrow = 3;
 // Decode work claimed at run time: this share (in 1/256) of the flattened blocks
 // goes to pieces of at least kMinPiece blocks (more than a ring holds) when static
 // ranges hold at least kMinPieceRange blocks; a claim is sent kClaimAhead blocks
@@ -74,6 +80,7 @@ struct DecodeParams {
     int block_shift;                  // log2(block_size)
     int num_workers;                  // warps taking part
     int dyn256;                       // share of the blocks in claimed pieces, in 1/256
+    int narrow;                       // 16-bit cache, two-stage ring (three CTAs per SM)
     unsigned* claim;                  // [0] piece counter, [1] its value when this call began
     int overlap_prior;                // nonzero: the previous launch is this call's chunk kernel,
                                       // which started only after its own predecessors finished;
@@ -160,9 +167,11 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
                                         int range_slots);
 
 // Decode kernels: dynamic shared memory for num_seqs sequences.
-size_t decode_smem_bytes(CacheKind kind, int num_seqs);
-cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t max_smem);
-cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, bool dyn, size_t smem, int* ctas_per_sm);
+// narrow: the 16-bit kernel with a two-stage ring per warp (three CTAs per SM)
+size_t decode_smem_bytes(CacheKind kind, int num_seqs, bool narrow);
+cudaError_t decode_prepare(CacheKind kind, bool q_bf16, bool append, bool dyn, bool narrow, size_t max_smem);
+cudaError_t decode_occupancy(CacheKind kind, bool q_bf16, bool append, bool dyn, bool narrow, size_t smem,
+                             int* ctas_per_sm);
 cudaError_t launch_decode(CacheKind kind, bool q_bf16, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, const DecodeParams& p, int grid, size_t smem,
                           cudaStream_t stream);
