@@ -152,7 +152,9 @@ PA_API size_t pa_workspace_size_shared_prefix(int num_seqs, int num_q_heads, int
 /* Default number of decode workers (warps) on the current device for a 16-bit
  * cache: two 4-warp CTAs per SM.  An FP8 cache defaults to twice as many (four
  * CTAs per SM: its warps are bound by the latency of the work on each block, not
- * by HBM).  Explicit worker counts run from 1 to this value for either. */
+ * by HBM); the 16-bit decode rows of pa_mixed and the private suffixes of
+ * pa_decode_shared_prefix run three CTAs per SM (shorter rings: those grids run
+ * beside another grid).  Explicit worker counts run from 1 to this value. */
 PA_API int pa_default_workers(void);
 
 /*
