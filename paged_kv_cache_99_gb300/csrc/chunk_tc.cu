@@ -18,16 +18,21 @@
 //                step's K blocks and V blocks (16-bit caches) into separate
 //                2-stage rings, one lane per block, K of step i+1 before V of i;
 //                it zeroes the V rows past the CTA's last key in the last step
-//   warp 1       one lane issues tcgen05.mma in a fixed order with suspending
-//                waits: per step O_A += P_A(i) V_i, S_A(i+1) = Q_A K_{i+1}^T, then
-//                the same for tile B (P read from tensor memory)
+//   warp 1       one lane issues tcgen05.mma in a fixed order: per step
+//                O_A += P_A(i) V_i, S_A(i+1) = Q_A K_{i+1}^T, then the same for
+//                tile B (P read from tensor memory).  With 16-bit caches it takes
+//                V_i and K_{i+1} before it waits for P, polls for P, and issues
+//                the P.V of a step's first 64 keys while the softmax still works
+//                on the other 64
 //   warps 2, 3   FP8 caches only: gather e4m3 rows through the block table,
 //                widen them exactly to f16 and store them in the MMA layout
 //   warps 4-7    softmax of tile A, warps 8-11 softmax of tile B: one thread
 //                per row holds its 128 scores in registers (one tensor-memory
 //                read per step), causal mask, online max/sum, P (16-bit)
-//                written back over the columns of S; O rescaled in tensor
-//                memory only when a row maximum grows by more than 2^8
+//                written back over the columns of S, with 16-bit caches released
+//                in two halves of 64 keys; O rescaled in tensor memory (before
+//                any of the step's P is released) only when a row maximum grows
+//                by more than 2^8
 // Warps 0-3 give registers to the softmax warpgroups (setmaxnreg).
 // Per tile the chain is S(i) -> softmax(i) -> P.V(i) -> S(i+1): S(i+1) reuses
 // the columns P(i) sits in, and the tensor core runs one thread's MMAs in
@@ -78,7 +83,8 @@ enum {
     kBarVEmpty = kBarVFull + kVStages,      // [V stage]
     kBarSFull = kBarVEmpty + kVStages,      // [tile]
     kBarPFull = kBarSFull + 2,              // [tile]
-    kBarPvDone = kBarPFull + 2,             // [tile]
+    kBarPHalf = kBarPFull + 2,              // [tile] 16-bit caches: P of the step's first 64 keys stored
+    kBarPvDone = kBarPHalf + 2,             // [tile]
     kBarQFull = kBarPvDone + 2,
     kBarVZero = kBarQFull + 1,              // 16-bit caches: V rows past the CTA's last key zeroed
     kNumBars = kBarVZero + 1
@@ -103,6 +109,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     ok = __shfl_sync(0xffffffffu, static_cast<int>(ok), 0) != 0;
     if (ok) mbar_try_wait(bar, parity);
     return ok;
+}
+
+// Bounded wait that polls with the non-suspending test: for the MMA issuer, which
+// must start the products the moment a softmax releases P.
+__device__ __forceinline__ bool mbar_poll_bounded(uint32_t bar, uint32_t parity, uint64_t limit) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int k = 0; k < 64; ++k)
+            if (mbar_test(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit) return false;
+    }
 }
 
 // Three-input maximum / minimum (one instruction on sm_100 and later).
@@ -162,6 +181,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(kBarSFull + x), 1);
             mbar_init(bar(kBarPFull + x), 4);
+            mbar_init(bar(kBarPHalf + x), 4);
             mbar_init(bar(kBarPvDone + x), 1);
         }
         mbar_init(bar(kBarQFull), 8);
@@ -382,22 +402,30 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     }
                     umma_commit(bar(kBarSFull + x));
                 };
-                auto issue_pv = [&](int x, int j) {
+                // P.V over keys 64 half .. 64 half + 63 (half = 0, 1), or all 128 (half = -1)
+                auto issue_pv = [&](int x, int j, int half) {
                     const uint32_t vbase = sbase + kOffV + (j % kVStages) * kKvBytes;
+                    const int kk0 = half > 0 ? kTcKeys / 32 : 0;
+                    const int kk1 = half == 0 ? kTcKeys / 32 : kTcKeys / 16;
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                        if (kk < kk0 || kk >= kk1) continue;
                         // V is MN-major: d-halves kKvHalf apart, 16 keys = 2 KiB
                         const uint64_t b = umma_desc_sw128(vbase + kk * 2048, kKvHalf, 1024);
                         umma_f16_ts(tO(x), tS(x) + 8 * kk, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 };
-                // Fixed order with suspending waits: per step, P.V(i) of A and A's S(i+1)
-                // right behind it (it reuses the columns P(i) sat in), then the same for B.
-                // Tile A runs about half a step ahead of B, so this is the order in which
-                // the inputs become ready; a waiting issuer sleeps instead of polling.
+                // Fixed order: per step, P.V(i) of A and A's S(i+1) right behind it (it
+                // reuses the columns P(i) sat in), then the same for B.  Tile A runs about
+                // half a step ahead of B, so this is the order in which the inputs become
+                // ready.
                 const int na = tile_steps(0), nb = tile_steps(1), nmax = na > nb ? na : nb;
                 auto wait = [&](uint32_t b, uint32_t par) -> bool {
                     if (ok && !mbar_wait_bounded(b, par, p.timeout_ns)) ok = false;
+                    return ok;
+                };
+                auto poll = [&](uint32_t b, uint32_t par) -> bool {
+                    if (ok && !mbar_poll_bounded(b, par, p.timeout_ns)) ok = false;
                     return ok;
                 };
                 if (wait(bar(kBarQFull), 0) && nmax > 0 && wait(bar(kBarKFull), 0)) {
@@ -408,16 +436,33 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 }
                 for (int i = 0; i < nmax && ok; ++i) {
                     const int sv = i % kVStages, sk = (i + 1) % kKStages;
+                    if constexpr (!kFp8) {
+                        // V_i and K_{i+1} are copied long before a softmax releases P(i):
+                        // take them first, so that nothing stands between P and its products
+                        if (!wait(bar(kBarVFull + sv), (i / kVStages) & 1) ||
+                            (i == nsteps - 1 && !wait(bar(kBarVZero), 0)) ||
+                            (i + 1 < nmax && !wait(bar(kBarKFull + sk), ((i + 1) / kKStages) & 1)))
+                            break;
+                    }
                     for (int x = 0; x < 2 && ok; ++x) {
                         if (i >= tile_steps(x)) continue;
-                        if (!wait(bar(kBarPFull + x), i & 1) || !wait(bar(kBarVFull + sv), (i / kVStages) & 1) ||
-                            (!kFp8 && i == nsteps - 1 && !wait(bar(kBarVZero), 0)))
-                            break;
-                        tc_fence_after();
-                        issue_pv(x, i);
+                        if constexpr (!kFp8) {
+                            // P.V of the first 64 keys while the softmax works on the rest
+                            if (!poll(bar(kBarPHalf + x), i & 1)) break;
+                            tc_fence_after();
+                            issue_pv(x, i, 0);
+                            if (!poll(bar(kBarPFull + x), i & 1)) break;
+                            tc_fence_after();
+                            issue_pv(x, i, 1);
+                        } else {
+                            // the converters widen K_{i+1} after V_i: K is taken after the P.V
+                            if (!wait(bar(kBarPFull + x), i & 1) || !wait(bar(kBarVFull + sv), (i / kVStages) & 1)) break;
+                            tc_fence_after();
+                            issue_pv(x, i, -1);
+                        }
                         if (i + 1 == tile_steps(x)) umma_commit(bar(kBarPvDone + x));
                         if (i + 1 < tile_steps(x)) {
-                            if (!wait(bar(kBarKFull + sk), ((i + 1) / kKStages) & 1)) break;
+                            if (kFp8 && !wait(bar(kBarKFull + sk), ((i + 1) / kKStages) & 1)) break;
                             tc_fence_after();
                             issue_s(x, i + 1);
                         }
@@ -596,6 +641,19 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             const float m_new = need ? fmaxf(m_used, mx) : m_used;
             const float alpha = ex2_approx(m_used - m_new);    // 0 on the first step, 1 when kept
             m_used = m_new;
+            // O is final for P.V(i-1): S(i) was issued after it and completes after it.
+            // Rescaled before any of P(i) is released, since P.V(i) accumulates into it.
+            if (i >= 1 && resc) {
+#pragma unroll 1
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO(x) + lane_off + 32 * c, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(tO(x) + lane_off + 32 * c, ov);
+                }
+            }
             // p = 2^(s * scale - m) as the 16-bit A operand of P.V, written over the
             // columns of S (keys 32 c .. +31 -> columns 16 c .. +15)
             // (s * scale - m) and the running sums two columns per instruction (f32x2)
@@ -620,17 +678,12 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                     pw[e >> 1] = pack2<kMmaBf16>(p0, p1);
                 }
                 tmem_st16(s_addr + 16 * c, pw);
-            }
-            // O is final for P.V(i-1): S(i) was issued after it and completes after it
-            if (i >= 1 && resc) {
-#pragma unroll 1
-                for (int c = 0; c < kHeadDim / 32; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO(x) + lane_off + 32 * c, ov);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st32(tO(x) + lane_off + 32 * c, ov);
+                if (!kFp8 && c == kTcKeys / 64 - 1) {
+                    // the first 64 keys' P (and any rescale of O) is in tensor memory
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kBarPHalf + x));
                 }
             }
             tmem_wait_st();
