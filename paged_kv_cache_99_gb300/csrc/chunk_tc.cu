@@ -197,6 +197,11 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
 
     const int B = p.num_seqs;
     const int QT = p.queries_per_tile;
+    // grid x = tile-pair slot x KV head, slot-major: every head's heaviest pair is
+    // dispatched first, and the slots past the batch's pairs (the host bounds the
+    // pair count without reading the query lengths) come last
+    const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.num_kv_heads));
+    const int slot = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.num_kv_heads));
     const bool prefix = p.prefix_keys > 0;
     int s = 0, pair = 0, q0 = 0, q_len = 0, n = 0;
     if (!prefix) {
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
                 run += w < warp ? warp_tot[w] : 0;
                 total += warp_tot[w];
             }
-            const int tau = total - 1 - static_cast<int>(blockIdx.x);   // heaviest pairs first
+            const int tau = total - 1 - slot;   // heaviest pairs first
             if (tau >= run && tau < run + local) {
                 for (int sq = beg; sq < end; ++sq) {
                     const int np = pairs_of(sq);
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
         // ---- prefix mode: query j is the decode row of sequence j; keys are the
         // shared prefix, read through sequence 0's table ----
         grid_launch_dependents();
-        pair = blockIdx.x;
+        pair = slot;
         q_len = B;
         n = p.prefix_keys;
         if (2 * pair * QT >= B) return;
@@ -266,7 +271,6 @@ __global__ void __launch_bounds__(TcCfg<Kind>::kWarps * 32, 1)
             return;
         }
     }
-    const int h = blockIdx.y;
     const int G = p.group;
     // position of query j: causal chunk rows follow the cached tokens; in prefix mode
     // every row sits after the whole prefix
@@ -796,7 +800,7 @@ cudaError_t chunk_prepare(CacheKind kind, bool q_bf16, size_t max_smem) {
 cudaError_t launch_chunk(CacheKind kind, bool q_bf16, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          const ChunkParams& p, int grid_x, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_x, p.num_kv_heads, p.prefix_keys > 0 && p.prefix_splits > 1 ? p.prefix_splits : 1);
+    cfg.gridDim = dim3(grid_x * p.num_kv_heads, 1, p.prefix_keys > 0 && p.prefix_splits > 1 ? p.prefix_splits : 1);
     cfg.blockDim = dim3(kind == kKindFp8 ? TcCfg<kKindFp8>::kWarps * 32 : TcCfg<kKindBf16>::kWarps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

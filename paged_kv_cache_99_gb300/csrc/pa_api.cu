@@ -323,7 +323,7 @@ pa_status chunk_impl(void* out, const void* q, const int32_t* query_start_loc, c
     // prefix mode: the queries are the sequences' decode rows, one tile pair per CTA
     const long long grid_x = prefix_units > 0 ? (num_seqs + per_cta - 1) / per_cta
                                                : static_cast<long long>(num_seqs) + (total_q + per_cta - 1) / per_cta;
-    if (grid_x >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    if (grid_x * num_kv_heads >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     ChunkParams p;
     p.out = out;
     p.q = q;
