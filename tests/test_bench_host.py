@@ -95,3 +95,28 @@ def test_step_hooks_wrap_each_layer_in_order():
     bench.build_step(wm, _RecordingPa(log), None, [torch.empty_like(wm.q[l]) for l in range(2)],
                      [(wm.k_cache[l], wm.v_cache[l]) for l in range(2)])
     assert log == ["pa_reshape_and_cache", "pa_mixed"] * 2
+
+
+def test_traffic_record_only_for_the_kernel_source_it_was_taken_on(tmp_path, monkeypatch):
+    # a record counts only while the kernel's sources hash to the value it was taken on
+    (tmp_path / "profiles").mkdir()
+    rec = {"wl-a": {"kernel_hash": "1" * 16, "dram_bytes_per_launch": 123},
+           "wl-b": {"kernel_hash": "0" * 16, "dram_bytes_per_launch": 456}}
+    (tmp_path / "profiles" / "chunk_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel="decode": "1" * 16)
+    assert bench.recorded_traffic("wl-a", "chunk") == 123
+    assert bench.recorded_traffic("wl-b", "chunk") is None      # stale: taken on other sources
+    assert bench.recorded_traffic("wl-c", "chunk") is None      # never recorded
+    assert bench.recorded_traffic("wl-a", "decode") is None     # no decode record file here
+
+
+def test_committed_traffic_records_name_their_sources():
+    # every committed record carries the hash it was taken on and a positive byte count
+    for kernel in ("decode", "chunk"):
+        with open(os.path.join(bench.ROOT, "profiles", f"{kernel}_traffic.json")) as f:
+            rec = json.load(f)
+        for name, ent in rec.items():
+            if name == "note":
+                continue
+            assert len(ent["kernel_hash"]) == 16 and ent["dram_bytes_per_launch"] > 0, (kernel, name)
