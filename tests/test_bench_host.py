@@ -1,5 +1,7 @@
 """Host-side pieces of the benchmark, on CPU: the algorithmic byte count, the
-max-over-ranks timing reduction across two gloo ranks, and the oracle arm."""
+max-over-ranks timing reduction across two gloo ranks, the oracle arm, and the
+rule that a DRAM-traffic record counts only for the kernel sources it was
+taken on."""
 import json
 import os
 import socket
