@@ -303,7 +303,8 @@ PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k
  *   out, q          device, [total_q][num_q_heads][128] of q_dtype
  *   query_start_loc device, int32 [num_seqs + 1], non-decreasing,
  *                   query_start_loc[0] == 0, query_start_loc[num_seqs] == total_q
- *   max_q_len       host upper bound of q_len_s (sizes the prefill grid)
+ *   max_q_len       host upper bound of q_len_s (0 or 1: no prefill chunks, the
+ *                   prefill kernel is not launched)
  * Other arguments as pa_decode.
  */
 PA_API pa_status pa_mixed(void* out, const void* q, const int32_t* query_start_loc, const void* k_cache,
